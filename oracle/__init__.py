@@ -1,0 +1,216 @@
+"""CPU oracle for fine-grained FP8 (E4M3) quantisation and the block-scaled GEMM.
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the CPU-baseline leg
+of the benchmark load it; the product path never does.  The arithmetic lives
+in ``oracle.c`` (plain C99, built with no fast-math and no FP contraction);
+this module only marshals numpy arrays into it.  Nothing here is shared with
+the CUDA library.
+
+Sources: "DeepSeek-V3 技术报告：从 671B MoE 到低成本训练系统" (xutianle.me)
+§6 (FP8 GEMMs for Fprop/Dgrad/Wgrad, outputs in BF16 or FP32), §6.1 (1x128
+activation tiles, 128x128 weight blocks, online scales), §6.2 (FP32 promotion
+after every 128 FP8 products).
+
+Parity pins: every function here is pinned by ``tests/test_oracle_*.py``
+against the format definition, torch's independent float8_e4m3fn
+conversion, exact rational brute force and closed-form identities.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+CFLAGS = ["-O2", "-std=c99", "-fno-fast-math", "-ffp-contract=off", "-fPIC",
+          "-shared", "-pthread", "-D_POSIX_C_SOURCE=200809L"]
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (gcc)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+        L.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+        L.orc_e4m3_decode.restype = ctypes.c_double
+        L.orc_e4m3_encode.argtypes = [ctypes.c_float]
+        L.orc_e4m3_encode.restype = ctypes.c_uint8
+        L.orc_bf16_rne.argtypes = [ctypes.c_float]
+        L.orc_bf16_rne.restype = ctypes.c_uint16
+        L.orc_tile_scale.argtypes = [ctypes.c_float]
+        L.orc_tile_scale.restype = ctypes.c_float
+        for fn in (L.orc_quant_1x128_rows, L.orc_quant_1x128_cols, L.orc_quant_128x128):
+            fn.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, i32]
+            fn.restype = None
+        L.orc_gemm_blockscaled.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i32,
+                                           i64, i64, vp, i64, vp, i32]
+        L.orc_gemm_blockscaled.restype = None
+        L.orc_bf16_round_buffer.argtypes = [vp, vp, i64]
+        L.orc_bf16_round_buffer.restype = None
+        L.orc_e4m3_encode_buffer.argtypes = [vp, vp, i64, i32]
+        L.orc_e4m3_encode_buffer.restype = None
+        L.orc_e4m3_encode_patterns.argtypes = [ctypes.c_uint64, i64, vp, i32]
+        L.orc_e4m3_encode_patterns.restype = None
+        _lib = L
+    return _lib
+
+
+def nthreads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    a = np.asarray(a)
+    assert a.dtype == dtype, (a.dtype, dtype)
+    return np.ascontiguousarray(a)
+
+
+# --- format ---------------------------------------------------------------
+
+def e4m3_decode(code: int) -> float:
+    return lib().orc_e4m3_decode(int(code))
+
+
+def e4m3_encode(y: float) -> int:
+    return int(lib().orc_e4m3_encode(float(np.float32(y))))
+
+
+def e4m3_encode_array(x: np.ndarray, threads: int | None = None) -> np.ndarray:
+    x = _c(x.astype(np.float32, copy=False), np.float32)
+    q = np.empty(x.shape, np.uint8)
+    lib().orc_e4m3_encode_buffer(_p(x), _p(q), x.size, threads or nthreads())
+    return q
+
+
+def e4m3_encode_patterns(lo: int, n: int, threads: int | None = None) -> np.ndarray:
+    """Encode the FP32 values whose bit patterns are lo, lo+1, ..., lo+n-1."""
+    q = np.empty(n, np.uint8)
+    lib().orc_e4m3_encode_patterns(lo, n, _p(q), threads or nthreads())
+    return q
+
+
+def decode_table() -> np.ndarray:
+    return np.array([e4m3_decode(c) for c in range(256)], dtype=np.float64)
+
+
+def tile_scale(amax: float) -> float:
+    return float(lib().orc_tile_scale(float(np.float32(amax))))
+
+
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    x = _c(x.astype(np.float32, copy=False), np.float32)
+    y = np.empty(x.shape, np.uint16)
+    lib().orc_bf16_round_buffer(_p(x), _p(y), x.size)
+    return y
+
+
+# --- quantisers -------------------------------------------------------------
+
+def quant_1x128_rows(x_bf16: np.ndarray, threads: int | None = None):
+    """x_bf16: uint16 [M, K].  Returns codes uint8 [M, K], scales f32 [K/128, M]."""
+    x = _c(x_bf16, np.uint16)
+    M, K = x.shape
+    assert K % 128 == 0
+    q = np.empty((M, K), np.uint8)
+    s = np.empty((K // 128, M), np.float32)
+    lib().orc_quant_1x128_rows(_p(x), M, K, K, _p(q), K, _p(s), M, threads or nthreads())
+    return q, s
+
+
+def quant_1x128_cols(x_bf16: np.ndarray, threads: int | None = None):
+    """x_bf16: uint16 [T, C]; tiles of 128 tokens per channel.
+    Returns codes uint8 [C, T] (tokens contiguous) and scales f32 [T/128, C]."""
+    x = _c(x_bf16, np.uint16)
+    T, C = x.shape
+    assert T % 128 == 0
+    q = np.empty((C, T), np.uint8)
+    s = np.empty((T // 128, C), np.float32)
+    lib().orc_quant_1x128_cols(_p(x), T, C, C, _p(q), T, _p(s), C, threads or nthreads())
+    return q, s
+
+
+def quant_128x128(w_bf16: np.ndarray, threads: int | None = None):
+    """w_bf16: uint16 [N, K].  Returns codes uint8 [N, K], scales f32 [ceil(N/128), K/128]."""
+    w = _c(w_bf16, np.uint16)
+    N, K = w.shape
+    assert K % 128 == 0
+    q = np.empty((N, K), np.uint8)
+    s = np.empty(((N + 127) // 128, K // 128), np.float32)
+    lib().orc_quant_128x128(_p(w), N, K, K, _p(q), K, _p(s), K // 128, threads or nthreads())
+    return q, s
+
+
+# --- GEMM -------------------------------------------------------------------
+
+def gemm_blockscaled(A: np.ndarray, sa: np.ndarray, B: np.ndarray, sb: np.ndarray,
+                     b_mode: int = 0, rows=None, threads: int | None = None) -> np.ndarray:
+    """FP32 accumulators of C = A * B^T with per-chunk FP32 promotion.
+
+    A: codes [M, K]; sa: [K/128, M]; B: codes [N, K];
+    sb: [ceil(N/128), K/128] (b_mode 0) or [K/128, N] (b_mode 1).
+    rows: optional list of row indices of A; returns f32 [len(rows), N]."""
+    A = _c(A, np.uint8)
+    B = _c(B, np.uint8)
+    sa = _c(sa, np.float32)
+    sb = _c(sb, np.float32)
+    M, K = A.shape
+    N, K2 = B.shape
+    assert K == K2 and K % 128 == 0
+    assert sa.shape == (K // 128, M)
+    if b_mode == 0:
+        assert sb.shape == ((N + 127) // 128, K // 128)
+    else:
+        assert sb.shape == (K // 128, N)
+    if rows is None:
+        rows = np.arange(M, dtype=np.int64)
+    rows = _c(np.asarray(rows, dtype=np.int64), np.int64)
+    out = np.empty((rows.size, N), np.float32)
+    lib().orc_gemm_blockscaled(_p(A), K, _p(sa), M, _p(B), K, _p(sb), sb.shape[1], b_mode,
+                               N, K, _p(rows), rows.size, _p(out), threads or nthreads())
+    return out
+
+
+def gemm_blockscaled_bf16(A, sa, B, sb, b_mode=0, rows=None, threads=None) -> np.ndarray:
+    """As gemm_blockscaled, rounded to BF16 bits (uint16)."""
+    return bf16_round(gemm_blockscaled(A, sa, B, sb, b_mode, rows, threads))
+
+
+def grouped_gemm(A: np.ndarray, sa: np.ndarray, B: np.ndarray, sb: np.ndarray,
+                 offsets: np.ndarray, rows=None, threads: int | None = None) -> np.ndarray:
+    """Grouped (MoE) GEMM: rows offsets[e]..offsets[e+1]-1 of A use expert e's
+    weights B[e] ([G, N, K]) and block scales sb[e] ([G, ceil(N/128), K/128]).
+    Returns FP32 accumulators for the requested rows (default: all), [len(rows), N]."""
+    offsets = np.asarray(offsets, dtype=np.int64)
+    G, N, K = B.shape
+    M = A.shape[0]
+    if rows is None:
+        rows = np.arange(M, dtype=np.int64)
+    rows = np.asarray(rows, dtype=np.int64)
+    out = np.empty((rows.size, N), np.float32)
+    expert_of = np.searchsorted(offsets, rows, side="right") - 1
+    for e in np.unique(expert_of):
+        sel = np.nonzero(expert_of == e)[0]
+        out[sel] = gemm_blockscaled(A, sa, B[e], sb[e], 0, rows[sel], threads)
+    return out
