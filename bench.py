@@ -1,0 +1,500 @@
+#!/usr/bin/env python3
+"""Benchmark: fine-grained FP8 (E4M3) quantise + block-scaled GEMM steps on B300.
+
+One step = one pass of the whole hot path over one batch of the workload:
+  mla   (default) A 4096x7168 BF16 -> 1x128 quantise; W_q 1536x7168 and
+        W_kv 576x7168 -> 128x128 quantise; two block-scaled GEMMs (BF16 out).
+  ffn   A 16384x7168 (Student-t), B 18432x7168: quantise both, one GEMM.
+  wgrad dY 16384x2048, X 16384x7168: token-wise 1x128 quantise (transposed
+        codes), dW = dY^T X with FP32 output.
+  moe   4096 tokens routed top-8 over 256 experts (32768 rows): quantise the
+        grouped rows, up grouped GEMM (N=4096, K=7168) with pre-quantised
+        expert weights.
+Inputs are seeded synthetic tensors (synth/), resident in HBM before timing.
+L2 is flushed (a 512 MB write) before every timed step, outside the step's
+CUDA events.  Prints one JSON line (rank 0).
+
+--impl reference times the CPU oracle (oracle/) on a bounded sample of the
+same workload instead: the method's plain restatement on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except OSError:
+        return dict(FALLBACK), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [l for (ts, l) in self.lines if t0 - 0.15 <= ts <= t1 + 0.15] or [l for _, l in self.lines]
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in rows:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+# ------------------------------------------------------------------ workloads
+def workload_desc(name):
+    return {
+        "mla": {"workload": "mla_down_proj", "M": 4096, "K": 7168, "N": [1536, 576],
+                "gemms": 2, "quant": "A 1x128, W_q/W_kv 128x128", "out": "bf16"},
+        "ffn": {"workload": "dense_ffn", "M": 16384, "K": 7168, "N": [18432],
+                "gemms": 1, "quant": "A 1x128, B 128x128", "out": "bf16"},
+        "wgrad": {"workload": "wgrad", "M": 2048, "K": 16384, "N": [7168],
+                  "gemms": 1, "quant": "dY, X 1x128 along tokens (transposed)", "out": "fp32"},
+        "moe": {"workload": "moe_grouped_up", "M": 32768, "K": 7168, "N": [4096], "experts": 256,
+                "topk": 8, "gemms": 1, "quant": "grouped rows 1x128 (weights pre-quantised)", "out": "bf16"},
+        "tiny": {"workload": "tiny", "M": 128, "K": 512, "N": [256], "gemms": 1,
+                 "quant": "A 1x128, B 128x128", "out": "bf16"},
+    }[name]
+
+
+def gemm_flops(name):
+    d = workload_desc(name)
+    return sum(2.0 * d["M"] * n * d["K"] for n in d["N"])
+
+
+def quant_bytes(name):
+    """Algorithmic HBM bytes of the step's quantisation: BF16 read + code
+    write + 4-byte scale per 128 elements (1x128) or per 128x128 block."""
+    d = workload_desc(name)
+    if name in ("mla", "ffn", "tiny"):
+        ea = d["M"] * d["K"]
+        ew = sum(d["N"]) * d["K"]
+        return ea * (3 + 4 / 128) + ew * (3 + 4 / (128 * 128))
+    if name == "wgrad":
+        e = d["K"] * (d["M"] + d["N"][0])
+        return e * (3 + 4 / 128)
+    if name == "moe":
+        return d["M"] * d["K"] * (3 + 4 / 128)
+    raise KeyError(name)
+
+
+class Step:
+    """Device buffers and the launch sequence of one step.  Every launch goes
+    through the C ABI (fp8_fine_grained_27_b300.binding)."""
+
+    def __init__(self, name, fb, torch, seed=0, rank=0):
+        import synth
+        self.name, self.fb, self.torch = name, fb, torch
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16).cuda()  # noqa: E731
+        self.kernels = []  # (label, kind) per launch, in order
+        if name in ("mla", "tiny"):
+            d = synth.mla(seed=seed) if name == "mla" else synth.tiny(seed=seed)
+            self.host = {"A": d["A"], "W": [d["Wq"], d["Wkv"]] if name == "mla" else [d["B"]]}
+        elif name == "ffn":
+            d = synth.ffn(seed=seed)
+            self.host = {"A": d["A"], "W": [d["B"]]}
+        elif name == "wgrad":
+            d = synth.wgrad(seed=seed)
+            self.host = {"dY": d["dY"], "X": d["X"]}
+        elif name == "moe":
+            tok = synth.moe_tokens(seed=seed)
+            offs, token_of_row = synth.moe_route(tok, seed=seed)
+            self.host = {"A": np.ascontiguousarray(tok[token_of_row]), "offs": offs}
+        self.d = {}
+        if name in ("mla", "tiny", "ffn"):
+            self.d["A"] = dev(self.host["A"])
+            self.d["W"] = [dev(w) for w in self.host["W"]]
+            M, K = self.host["A"].shape
+            self.d["qa"] = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+            self.d["sa"] = torch.empty((K // 128, M), dtype=torch.float32, device="cuda")
+            self.d["qw"] = [torch.empty_like(w, dtype=torch.uint8) for w in self.d["W"]]
+            self.d["sw"] = [torch.empty(((w.shape[0] + 127) // 128, K // 128), dtype=torch.float32, device="cuda")
+                            for w in self.d["W"]]
+            self.d["C"] = [torch.empty((M, w.shape[0]), dtype=torch.bfloat16, device="cuda") for w in self.d["W"]]
+        elif name == "wgrad":
+            self.d["dY"], self.d["X"] = dev(self.host["dY"]), dev(self.host["X"])
+            T, Co = self.host["dY"].shape
+            Ci = self.host["X"].shape[1]
+            self.d["qdy"] = torch.empty((Co, T), dtype=torch.uint8, device="cuda")
+            self.d["sdy"] = torch.empty((T // 128, Co), dtype=torch.float32, device="cuda")
+            self.d["qx"] = torch.empty((Ci, T), dtype=torch.uint8, device="cuda")
+            self.d["sx"] = torch.empty((T // 128, Ci), dtype=torch.float32, device="cuda")
+            self.d["C"] = [torch.empty((Co, Ci), dtype=torch.float32, device="cuda")]
+        elif name == "moe":
+            self.d["A"] = dev(self.host["A"])
+            M, K = self.host["A"].shape
+            G, N = 256, 4096
+            self.d["qa"] = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+            self.d["sa"] = torch.empty((K // 128, M), dtype=torch.float32, device="cuda")
+            self.d["qb"] = torch.empty((G, N, K), dtype=torch.uint8, device="cuda")
+            self.d["sb"] = torch.empty((G, N // 128, K // 128), dtype=torch.float32, device="cuda")
+            for e0 in range(0, G, 16):  # expert weights: quantised once, outside the step
+                w = dev(synth.moe_weights("up", e0, e0 + 16, seed=seed))
+                fb.quant_128x128(w.reshape(16 * N, K), q=self.d["qb"][e0:e0 + 16].view(16 * N, K),
+                                 s=self.d["sb"][e0:e0 + 16].view(16 * N // 128, K // 128))
+                del w
+            self.d["offs"] = torch.from_numpy(self.host["offs"].astype(np.int32)).cuda()
+            self.d["C"] = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda")]
+        torch.cuda.synchronize()
+
+    def launches(self):
+        """Return [(label, callable)] for one step."""
+        fb, d = self.fb, self.d
+        if self.name in ("mla", "tiny", "ffn"):
+            L = [("quant_1x128", lambda: fb.quant_1x128(d["A"], q=d["qa"], s=d["sa"]))]
+            for i in range(len(d["W"])):
+                L.append(("quant_128x128", lambda i=i: fb.quant_128x128(d["W"][i], q=d["qw"][i], s=d["sw"][i])))
+            for i in range(len(d["W"])):
+                L.append(("gemm", lambda i=i: fb.gemm_blockscaled(d["qa"], d["sa"], d["qw"][i], d["sw"][i], 0,
+                                                                  C=d["C"][i])))
+            return L
+        if self.name == "wgrad":
+            return [("quant_1x128_cols", lambda: fb.quant_1x128(d["dY"], along=1, q=d["qdy"], s=d["sdy"])),
+                    ("quant_1x128_cols", lambda: fb.quant_1x128(d["X"], along=1, q=d["qx"], s=d["sx"])),
+                    ("gemm", lambda: fb.gemm_blockscaled(d["qdy"], d["sdy"], d["qx"], d["sx"], 1, C=d["C"][0]))]
+        if self.name == "moe":
+            return [("quant_1x128", lambda: fb.quant_1x128(d["A"], q=d["qa"], s=d["sa"])),
+                    ("gemm", lambda: fb.grouped_gemm_moe(d["qa"], d["sa"], d["qb"], d["sb"], d["offs"],
+                                                         C=d["C"][0]))]
+        raise KeyError(self.name)
+
+    def host_inputs(self):
+        """(name, host array) of this step's BF16 inputs, for the end-to-end run."""
+        if self.name in ("mla", "tiny", "ffn"):
+            return [("A", self.host["A"])] + [(f"W{i}", w) for i, w in enumerate(self.host["W"])]
+        if self.name == "wgrad":
+            return [("dY", self.host["dY"]), ("X", self.host["X"])]
+        return [("A", self.host["A"])]
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world):
+    import torch
+
+    import fp8_fine_grained_27_b300 as fb
+    fb.lib()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    step = Step(args.workload, fb, torch, seed=rank)
+    launches = step.launches()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        for _, f in launches:
+            f()
+    torch.cuda.synchronize()
+    if fb.get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    nk = len(launches)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for k in range(args.steps):
+        flush.zero_()
+        ev[k][0].record(stream)
+        for j, (_, f) in enumerate(launches):
+            f()
+            ev[k][j + 1].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1)
+    if fb.get_device_error() != 0:
+        raise RuntimeError("device error during the timed region")
+
+    per_step = [ev[k][0].elapsed_time(ev[k][nk]) for k in range(args.steps)]
+    per_kernel = {}
+    for k in range(args.steps):
+        for j, (label, _) in enumerate(launches):
+            per_kernel.setdefault(label, []).append(ev[k][j].elapsed_time(ev[k][j + 1]))
+    ms_step = float(np.mean(per_step))
+    if dist:
+        t = torch.tensor([ms_step], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    flops = gemm_flops(args.workload)
+    qbytes = quant_bytes(args.workload)
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    peaks, peaks_src = load_peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    # GEMM launches of one step (there may be several): their summed mean duration
+    g_idx = [j for j, (l, _) in enumerate(launches) if l == "gemm"]
+    gemm_ms = float(np.mean([sum(ev[k][j].elapsed_time(ev[k][j + 1]) for j in g_idx) for k in range(args.steps)]))
+    q_idx = [j for j, (l, _) in enumerate(launches) if l != "gemm"]
+    quant_ms = float(np.mean([sum(ev[k][j].elapsed_time(ev[k][j + 1]) for j in q_idx) for k in range(args.steps)]))
+    achieved = flops / (gemm_ms * 1e-3) / 1e12
+    quant_gbs = qbytes / (quant_ms * 1e-3) / 1e9
+
+    e2e = run_e2e(args, step, torch, fb, launches, flops, world, dist)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = run_cpu_baseline(args.workload, budget_s=args.cpu_budget)
+
+    line = {
+        "metric": "block-scaled FP8 GEMM TFLOPS (% of B300 FP8 peak); quantize GB/s (% HBM)",
+        "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> fp32 accumulate",
+        "data": "synthetic (seeded; shapes of the DeepSeek-V3 pages)",
+        "config": {**workload_desc(args.workload), "l2": "flushed (512 MB write) before every step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(fp8_peak, 1),
+                     "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4), "traffic": None,
+                     "peak_source": f"{peaks_src}: 2 x bf16_tflops (dense FP8 = 2 x BF16)",
+                     "kernel": "gemm_kernel", "kernel_ms": round(gemm_ms, 5)},
+        "quant": {"achieved_gbs": round(quant_gbs, 1), "peak_gbs": peaks["hbm_gbs"],
+                  "frac": round(quant_gbs / peaks["hbm_gbs"], 4), "kernel_ms": round(quant_ms, 5),
+                  "bytes_per_step": int(qbytes)},
+        "per_kernel_ms": {l: round(float(np.mean(v)), 5) for l, v in per_kernel.items()},
+        "e2e": e2e,
+        "gpu_launches": nk * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": round(t1 - t0, 3),
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, step, torch, fb, launches, flops, world, dist):
+    """Same metric through the public API with host buffers: pinned H2D of the
+    step's BF16 inputs, the step's launches, D2H of the outputs, per step."""
+    pinned = [(n, torch.from_numpy(np.ascontiguousarray(a)).pin_memory()) for n, a in step.host_inputs()]
+    outs = step.d["C"]
+    out_host = [torch.empty(c.shape, dtype=c.dtype).pin_memory() for c in outs]
+    targets = {}
+    if step.name in ("mla", "tiny", "ffn"):
+        targets = {"A": step.d["A"], **{f"W{i}": w for i, w in enumerate(step.d["W"])}}
+    elif step.name == "wgrad":
+        targets = {"dY": step.d["dY"], "X": step.d["X"]}
+    else:
+        targets = {"A": step.d["A"]}
+    h2d = sum(p.numel() * p.element_size() for _, p in pinned)
+    d2h = sum(o.numel() * o.element_size() for o in out_host)
+    n = max(3, min(args.e2e_steps, args.steps))
+    for _ in range(2):
+        for name, p in pinned:
+            targets[name].view(torch.int16).copy_(p.view(torch.int16), non_blocking=True)
+        for _, f in launches:
+            f()
+        for o, h in zip(outs, out_host):
+            h.copy_(o, non_blocking=True)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        for name, p in pinned:
+            targets[name].view(torch.int16).copy_(p.view(torch.int16), non_blocking=True)
+        for _, f in launches:
+            f()
+        for o, h in zip(outs, out_host):
+            h.copy_(o, non_blocking=True)
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / n
+    if dist:
+        t = torch.tensor([dt], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dt = float(t.item())
+    return {"value": round(world * flops / dt / 1e12, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": n, "ms_per_step": round(dt * 1e3, 4)}
+
+
+# ------------------------------------------------------------------ oracle arm
+def oracle_sample(workload, seed=0):
+    """A bounded sample of one step for the CPU oracle: (work fn, flops, description)."""
+    import oracle
+    import synth
+    oracle.build()
+    if workload in ("mla", "tiny"):
+        d = synth.mla(seed=seed) if workload == "mla" else synth.tiny(seed=seed)
+        Ws = [d["Wq"], d["Wkv"]] if workload == "mla" else [d["B"]]
+        rows = 32 if workload == "mla" else 128
+        A = np.ascontiguousarray(d["A"][:rows])
+
+        def work():
+            qa, sa = oracle.quant_1x128_rows(A)
+            for W in Ws:
+                qb, sb = oracle.quant_128x128(W)
+                oracle.gemm_blockscaled(qa, sa, qb, sb, 0)
+        flops = sum(2.0 * rows * W.shape[0] * W.shape[1] for W in Ws)
+        return work, flops, f"{rows} of {d['A'].shape[0]} rows of A (quantise + both GEMMs) plus full weight quantisation"
+    if workload == "ffn":
+        d = synth.ffn(seed=seed, M=16, N=18432)
+        A, B = d["A"], d["B"][:2048]
+
+        def work():
+            qa, sa = oracle.quant_1x128_rows(A)
+            qb, sb = oracle.quant_128x128(B)
+            oracle.gemm_blockscaled(qa, sa, qb, sb, 0)
+        return work, 2.0 * 16 * 2048 * 7168, "16 rows x 2048 columns of the 16384x18432x7168 GEMM, with their quantisation"
+    if workload == "wgrad":
+        d = synth.wgrad(seed=seed)
+        dY, X = d["dY"][:, :16], d["X"][:, :512]
+        dY, X = np.ascontiguousarray(dY), np.ascontiguousarray(X)
+
+        def work():
+            qd, sd = oracle.quant_1x128_cols(dY)
+            qx, sx = oracle.quant_1x128_cols(X)
+            oracle.gemm_blockscaled(qd, sd, qx, sx, 1)
+        return work, 2.0 * 16 * 512 * 16384, "16 x 512 outputs of dW (K = 16384 tokens), with their token-wise quantisation"
+    if workload == "moe":
+        tok = synth.moe_tokens(seed=seed, T=64)
+        W = synth.moe_weights("up", 0, 1, seed=seed)[0][:1024]
+
+        def work():
+            qa, sa = oracle.quant_1x128_rows(tok)
+            qb, sb = oracle.quant_128x128(W)
+            oracle.gemm_blockscaled(qa, sa, qb, sb, 0)
+        return work, 2.0 * 64 * 1024 * 7168, "64 rows x 1024 columns of one expert's up GEMM, with quantisation"
+    raise KeyError(workload)
+
+
+def run_cpu_baseline(workload, budget_s=20.0):
+    import oracle
+    work, flops, desc = oracle_sample(workload)
+    work()  # first call builds tables
+    reps, t = 0, 0.0
+    t0 = time.perf_counter()
+    while True:
+        work()
+        reps += 1
+        t = time.perf_counter() - t0
+        if t > budget_s or reps >= 50:
+            break
+    return {"value": round(flops * reps / t / 1e12, 8), "unit": "TFLOP/s", "cores": oracle.nthreads(),
+            "kind": "oracle", "sample": desc, "reps": reps, "seconds": round(t, 2)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    work, flops, desc = oracle_sample(args.workload)
+    import oracle
+    for _ in range(args.warmup):
+        work()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        work()
+        times.append(time.perf_counter() - t0)
+    ms = float(np.mean(times)) * 1e3
+    value = flops / (ms * 1e-3) / 1e12
+    line = {
+        "impl": "reference",
+        "metric": "block-scaled FP8 GEMM TFLOPS (% of B300 FP8 peak); quantize GB/s (% HBM)",
+        "value": round(value, 8), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 codes, f64 chunk sums, f32 promotion", "data": "synthetic (seeded)",
+        "config": workload_desc(args.workload),
+        "cpu_baseline": {"value": round(value, 8), "unit": "TFLOP/s", "cores": oracle.nthreads(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 8), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--workload", default="mla", choices=["mla", "ffn", "wgrad", "moe", "tiny"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", args.gpus))
+    if args.impl == "reference":
+        args.steps = args.steps or 5
+        args.warmup = args.warmup if args.warmup is not None else 1
+        run_reference(args, rank, world)
+        return
+    default_steps = {"mla": 10000, "tiny": 10000, "ffn": 200, "wgrad": 1000, "moe": 300}[args.workload]
+    args.steps = args.steps or default_steps
+    args.warmup = max(3, args.warmup if args.warmup is not None else 20)
+    run_ours(args, rank, world)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,18 @@
+"""Fine-grained FP8 (E4M3) block-scaled GEMM for B300 (sm_103a).
+
+The compute lives in ``libfp8bs.so`` (hand-written CUDA: tile quantisers and
+tcgen05 GEMMs, C ABI in ``include/fp8bs.h``); :mod:`.binding` marshals torch
+tensors into it.  There is no CPU path: if the library is missing the import
+of the binding fails.
+"""
+from .binding import (  # noqa: F401
+    Fp8bsError,
+    e4m3_encode,
+    gemm_blockscaled,
+    get_device_error,
+    grouped_gemm_moe,
+    lib,
+    quant_1x128,
+    quant_128x128,
+    selftest_timeout,
+)

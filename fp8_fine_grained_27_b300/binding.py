@@ -1,0 +1,146 @@
+"""ctypes binding of libfp8bs (argument marshalling only).
+
+Each function takes torch CUDA tensors, allocates missing outputs with torch
+(device memory is the caller's), and calls the C entry point of the same
+name on the current torch stream.  All arithmetic happens in the library's
+kernels; a non-zero status raises :class:`Fp8bsError`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfp8bs.so")
+
+OK, EINVAL, EALIGN, EARCH, ECUDA, ETIMEOUT = 0, -1, -2, -3, -4, -5
+
+# every symbol include/fp8bs.h declares
+EXPORTS = (
+    "fp8_quant_1x128", "fp8_quant_128x128", "fp8_gemm_blockscaled", "fp8_grouped_gemm_moe",
+    "fp8bs_e4m3_encode", "fp8bs_status_string", "fp8bs_get_device_error",
+    "fp8bs_selftest_timeout", "fp8bs_version",
+)
+
+
+class Fp8bsError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {lib().fp8bs_status_string(status).decode()} ({status})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libfp8bs.so (built in-tree by __graft_entry__.build or build.py)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libfp8bs.so is not built ({LIB_PATH}); run fp8_fine_grained_27_b300/build.py")
+        L = ctypes.CDLL(LIB_PATH)
+        i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+        L.fp8_quant_1x128.argtypes = [vp, i64, i64, i64, i32, vp, i64, vp, i64, vp]
+        L.fp8_quant_128x128.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp]
+        L.fp8_gemm_blockscaled.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i32, vp, i64, i32, i64, i64, i64, vp]
+        L.fp8_grouped_gemm_moe.argtypes = [vp, i64, vp, i64, vp, vp, vp, i32, i64, vp, i64, i32, i64, i64, vp]
+        L.fp8bs_e4m3_encode.argtypes = [vp, vp, i64, vp]
+        L.fp8bs_status_string.argtypes = [i32]
+        L.fp8bs_status_string.restype = ctypes.c_char_p
+        L.fp8bs_get_device_error.argtypes = [vp]
+        L.fp8bs_selftest_timeout.argtypes = [i64, vp]
+        L.fp8bs_version.restype = ctypes.c_char_p
+        for name in ("fp8_quant_1x128", "fp8_quant_128x128", "fp8_gemm_blockscaled",
+                     "fp8_grouped_gemm_moe", "fp8bs_e4m3_encode", "fp8bs_get_device_error",
+                     "fp8bs_selftest_timeout"):
+            getattr(L, name).restype = i32
+        _lib = L
+    return _lib
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _check(fn, rc):
+    if rc != OK:
+        raise Fp8bsError(fn, rc)
+
+
+def _ld(t: torch.Tensor) -> int:
+    assert t.dim() == 2 and t.stride(1) == 1, "row-major matrix with unit column stride expected"
+    return t.stride(0)
+
+
+def quant_1x128(x: torch.Tensor, along: int = 0, q=None, s=None, stream=None):
+    """1x128 tile quantisation of BF16 x [M, K].
+    along=0: q [M, K] codes, s [K/128, M];  along=1: q [K, M] codes, s [M/128, K]."""
+    M, K = x.shape
+    if along == 0:
+        q = torch.empty((M, K), dtype=torch.uint8, device=x.device) if q is None else q
+        s = torch.empty((K // 128, M), dtype=torch.float32, device=x.device) if s is None else s
+    else:
+        q = torch.empty((K, M), dtype=torch.uint8, device=x.device) if q is None else q
+        s = torch.empty((M // 128, K), dtype=torch.float32, device=x.device) if s is None else s
+    _check("fp8_quant_1x128", lib().fp8_quant_1x128(_ptr(x), M, K, _ld(x), along, _ptr(q), _ld(q),
+                                                    _ptr(s), _ld(s), _stream(stream)))
+    return q, s
+
+
+def quant_128x128(w: torch.Tensor, q=None, s=None, stream=None):
+    """128x128 block quantisation of BF16 w [N, K]: q [N, K], s [ceil(N/128), K/128]."""
+    N, K = w.shape
+    q = torch.empty((N, K), dtype=torch.uint8, device=w.device) if q is None else q
+    s = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=w.device) if s is None else s
+    _check("fp8_quant_128x128", lib().fp8_quant_128x128(_ptr(w), N, K, _ld(w), _ptr(q), _ld(q),
+                                                        _ptr(s), _ld(s), _stream(stream)))
+    return q, s
+
+
+def gemm_blockscaled(A, sa, B, sb, b_scale_mode: int = 0, out_dtype=torch.bfloat16, C=None, stream=None):
+    """C = A * B^T with fine-grained scales (FP32 promotion every 128 K)."""
+    M, K = A.shape
+    N = B.shape[0]
+    if C is None:
+        C = torch.empty((M, N), dtype=out_dtype, device=A.device)
+    od = 0 if C.dtype == torch.bfloat16 else 1
+    _check("fp8_gemm_blockscaled", lib().fp8_gemm_blockscaled(
+        _ptr(A), _ld(A), _ptr(sa), _ld(sa), _ptr(B), _ld(B), _ptr(sb), _ld(sb), b_scale_mode,
+        _ptr(C), _ld(C), od, M, N, K, _stream(stream)))
+    return C
+
+
+def grouped_gemm_moe(A, sa, B, sb, offsets, out_dtype=torch.bfloat16, C=None, stream=None):
+    """Per-expert GEMMs: A [M_total, K] codes (expert-sorted), B [G, N, K], sb [G, ceil(N/128), K/128],
+    offsets int32 [G+1] on the device."""
+    M, K = A.shape
+    G, N, K2 = B.shape
+    assert K == K2 and B.is_contiguous() and sb.is_contiguous() and offsets.dtype == torch.int32
+    if C is None:
+        C = torch.empty((M, N), dtype=out_dtype, device=A.device)
+    od = 0 if C.dtype == torch.bfloat16 else 1
+    _check("fp8_grouped_gemm_moe", lib().fp8_grouped_gemm_moe(
+        _ptr(A), _ld(A), _ptr(sa), _ld(sa), _ptr(B), _ptr(sb), _ptr(offsets), G, M,
+        _ptr(C), _ld(C), od, N, K, _stream(stream)))
+    return C
+
+
+def e4m3_encode(x: torch.Tensor, q=None, stream=None):
+    q = torch.empty(x.shape, dtype=torch.uint8, device=x.device) if q is None else q
+    _check("fp8bs_e4m3_encode", lib().fp8bs_e4m3_encode(_ptr(x), _ptr(q), x.numel(), _stream(stream)))
+    return q
+
+
+def get_device_error(stream=None) -> int:
+    return lib().fp8bs_get_device_error(_stream(stream))
+
+
+def selftest_timeout(timeout_ns: int, stream=None):
+    _check("fp8bs_selftest_timeout", lib().fp8bs_selftest_timeout(timeout_ns, _stream(stream)))

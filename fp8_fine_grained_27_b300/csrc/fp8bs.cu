@@ -1,0 +1,401 @@
+// fp8bs.cu -- the C ABI of libfp8bs (declared in include/fp8bs.h): argument
+// checks, TMA descriptors and kernel launches for the E4M3 quantisers and
+// the block-scaled GEMMs.  Single translation unit; sm_103a only.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fp8bs.h"
+#include "gemm.cuh"
+#include "ptx.cuh"
+#include "quant.cuh"
+
+namespace fp8bs {
+
+// A barrier nothing completes, waited on with a short bound: exercises the
+// timeout path of every kernel without faulting or hanging.
+__global__ void selftest_timeout_kernel(uint64_t limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t a = smem_addr(&bar);
+    if (threadIdx.x == 0)
+        mbar_init(a, 1);
+    __syncthreads();
+    if (threadIdx.x == 0)
+        mbar_wait(a, 0, ERR_TIMEOUT_SELFTEST, limit_ns);
+    __syncthreads();
+}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool init = false;
+    bool sm103 = false;
+    int num_sms = 0;
+    int quant_rows_ctas = 0;  // resident CTAs per SM, 1x128 and 128x128 kernels
+    int quant_block_ctas = 0;
+    int quant_cols_ctas = 0;
+    unsigned gemm_attr_set = 0;  // bit per GEMM instance: smem attribute applied
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int current_device(DeviceInfo **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return FP8BS_ECUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.init) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return FP8BS_ECUDA;
+        d.sm103 = (major == 10 && minor == 3);
+        d.num_sms = sms;
+        if (d.sm103) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.quant_rows_ctas, quant::quant_rows_kernel<false>,
+                                                              quant::kThreads, 0) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.quant_block_ctas, quant::quant_rows_kernel<true>,
+                                                              quant::kThreads, 0) != cudaSuccess)
+                return FP8BS_ECUDA;
+            if (cudaFuncSetAttribute(quant::quant_cols_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     sizeof(quant::ColsSmem)) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.quant_cols_ctas, quant::quant_cols_kernel,
+                                                              quant::kThreads, sizeof(quant::ColsSmem)) != cudaSuccess)
+                return FP8BS_ECUDA;
+            if (!g_encode) {
+                void *fn = nullptr;
+                cudaDriverEntryPointQueryResult q;
+                if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                        cudaSuccess ||
+                    q != cudaDriverEntryPointSuccess || !fn)
+                    return FP8BS_ECUDA;
+                g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+            }
+        }
+        d.init = true;
+    }
+    if (!d.sm103)
+        return FP8BS_EARCH;
+    *out = &d;
+    return FP8BS_OK;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int launch_status()
+{
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? FP8BS_OK : FP8BS_ECUDA;
+}
+
+// 2D tensor map over a row-major matrix: `cols` contiguous elements per row,
+// `rows` rows, row pitch `ld_bytes`; box = box_cols x box_rows.
+int make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t cols, uint64_t rows,
+             uint64_t ld_bytes, uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle sw)
+{
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {ld_bytes};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8BS_OK : FP8BS_EINVAL;
+}
+
+// ------------------------------------------------------------------ GEMM
+template <int BN, int STAGES, int BMODE, bool OUT_F32, bool GROUPED>
+int launch_gemm(DeviceInfo *d, int inst_bit, const CUtensorMap &tA, const CUtensorMap &tB, const CUtensorMap &tSB,
+                const gemm::Params &p, int grid, cudaStream_t st)
+{
+    using L = gemm::Layout<BN, STAGES, BMODE>;
+    auto kern = gemm::gemm_kernel<BN, STAGES, BMODE, OUT_F32, GROUPED>;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!(d->gemm_attr_set & (1u << inst_bit))) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
+                return FP8BS_ECUDA;
+            d->gemm_attr_set |= (1u << inst_bit);
+        }
+    }
+    kern<<<grid, gemm::kThreads, L::ALLOC, st>>>(tA, tB, tSB, p);
+    return launch_status();
+}
+
+}  // namespace
+}  // namespace fp8bs
+
+using namespace fp8bs;
+
+extern "C" {
+
+const char *fp8bs_version(void) { return "fp8bs 0.1 (sm_103a, tcgen05)"; }
+
+const char *fp8bs_status_string(int status)
+{
+    switch (status) {
+    case FP8BS_OK: return "ok";
+    case FP8BS_EINVAL: return "invalid argument";
+    case FP8BS_EALIGN: return "pointer or pitch not 16-byte aligned";
+    case FP8BS_EARCH: return "device is not sm_103";
+    case FP8BS_ECUDA: return "CUDA error";
+    case FP8BS_ETIMEOUT: return "kernel abandoned a bounded wait";
+    default: return "unknown status";
+    }
+}
+
+int fp8_quant_1x128(const void *x, int64_t M, int64_t K, int64_t ldx, int along, uint8_t *q, int64_t ldq, float *s,
+                    int64_t lds, void *stream)
+{
+    if (M < 0 || K < 0 || (along != 0 && along != 1))
+        return FP8BS_EINVAL;
+    if (M == 0 || K == 0)
+        return FP8BS_OK;
+    if (!x || !q || !s || ldx < K)
+        return FP8BS_EINVAL;
+    if (M > (int64_t(1) << 31) || K > (int64_t(1) << 31))
+        return FP8BS_EINVAL;
+    if (!aligned16(x) || !aligned16(q) || (ldx * 2) % 16 != 0 || ldq % 16 != 0)
+        return FP8BS_EALIGN;
+    DeviceInfo *d;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (along == 0) {
+        if (K % 128 != 0 || ldq < K || lds < M)
+            return FP8BS_EINVAL;
+        const int64_t tiles = ((M + 127) / 128) * (K / 128);
+        const int64_t grid = std::min<int64_t>(tiles, int64_t(d->num_sms) * d->quant_rows_ctas);
+        quant::quant_rows_kernel<false><<<static_cast<int>(grid), quant::kThreads, 0, st>>>(
+            static_cast<const uint16_t *>(x), M, K, ldx, q, ldq, s, lds);
+    } else {
+        if (M % 128 != 0 || K % 8 != 0 || ldq < M || lds < K)
+            return FP8BS_EINVAL;
+        const int64_t tiles = (M / 128) * ((K + 127) / 128);
+        const int64_t grid = std::min<int64_t>(tiles, int64_t(d->num_sms) * d->quant_cols_ctas);
+        quant::quant_cols_kernel<<<static_cast<int>(grid), quant::kThreads, sizeof(quant::ColsSmem), st>>>(
+            static_cast<const uint16_t *>(x), M, K, ldx, q, ldq, s, lds);
+    }
+    return launch_status();
+}
+
+int fp8_quant_128x128(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq, float *s,
+                      int64_t lds, void *stream)
+{
+    if (N < 0 || K < 0)
+        return FP8BS_EINVAL;
+    if (N == 0 || K == 0)
+        return FP8BS_OK;
+    if (!w || !q || !s || ldw < K || ldq < K || K % 128 != 0 || lds < K / 128)
+        return FP8BS_EINVAL;
+    if (N > (int64_t(1) << 31) || K > (int64_t(1) << 31))
+        return FP8BS_EINVAL;
+    if (!aligned16(w) || !aligned16(q) || (ldw * 2) % 16 != 0 || ldq % 16 != 0)
+        return FP8BS_EALIGN;
+    DeviceInfo *d;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK)
+        return rc;
+    const int64_t tiles = ((N + 127) / 128) * (K / 128);
+    const int64_t grid = std::min<int64_t>(tiles, int64_t(d->num_sms) * d->quant_block_ctas);
+    quant::quant_rows_kernel<true><<<static_cast<int>(grid), quant::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(w), N, K, ldw, q, ldq, s, lds);
+    return launch_status();
+}
+
+static int gemm_common_checks(const uint8_t *A, int64_t lda, const float *sa, int64_t ldsa, const uint8_t *B,
+                              const float *sb, void *C, int64_t ldc, int out_dtype, int64_t M, int64_t N, int64_t K)
+{
+    if (M < 0 || N < 0 || K < 0 || (out_dtype != 0 && out_dtype != 1))
+        return FP8BS_EINVAL;
+    if (M == 0 || N == 0)
+        return 1;  // nothing to do
+    if (K == 0 || K % 128 != 0 || N % 8 != 0 || !A || !sa || !B || !sb || !C)
+        return FP8BS_EINVAL;
+    if (M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31) || K >= (int64_t(1) << 31))
+        return FP8BS_EINVAL;
+    if (lda < K || ldsa < M || ldc < N)
+        return FP8BS_EINVAL;
+    const int esize = out_dtype == 0 ? 2 : 4;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || lda % 16 != 0 || (ldc * esize) % 16 != 0 ||
+        (reinterpret_cast<uintptr_t>(sa) & 3) || (reinterpret_cast<uintptr_t>(sb) & 3))
+        return FP8BS_EALIGN;
+    return 0;
+}
+
+int fp8_gemm_blockscaled(const uint8_t *A, int64_t lda, const float *sa, int64_t ldsa, const uint8_t *B, int64_t ldb,
+                         const float *sb, int64_t ldsb, int b_scale_mode, void *C, int64_t ldc, int out_dtype,
+                         int64_t M, int64_t N, int64_t K, void *stream)
+{
+    if (b_scale_mode != 0 && b_scale_mode != 1)
+        return FP8BS_EINVAL;
+    int rc = gemm_common_checks(A, lda, sa, ldsa, B, sb, C, ldc, out_dtype, M, N, K);
+    if (rc < 0)
+        return rc;
+    if (rc == 1)
+        return FP8BS_OK;
+    if (ldb < K)
+        return FP8BS_EINVAL;
+    if (ldb % 16 != 0)
+        return FP8BS_EALIGN;
+    if (b_scale_mode == 0 && ldsb < K / 128)
+        return FP8BS_EINVAL;
+    if (b_scale_mode == 1) {
+        if (ldsb < N)
+            return FP8BS_EINVAL;
+        if (ldsb % 4 != 0 || !aligned16(sb))
+            return FP8BS_EALIGN;
+    }
+    DeviceInfo *d;
+    rc = current_device(&d);
+    if (rc != FP8BS_OK)
+        return rc;
+
+    gemm::Params p;
+    p.sa = sa;
+    p.ldsa = ldsa;
+    p.sb = sb;
+    p.ldsb = ldsb;
+    p.sb_estride = 0;
+    p.C = C;
+    p.ldc = ldc;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.offs = nullptr;
+    p.G = 0;
+
+    const bool wide = (b_scale_mode == 0) && N > 128;
+    const int BN = wide ? 256 : 128;
+    CUtensorMap tA, tB, tSB;
+    std::memset(&tSB, 0, sizeof tSB);
+    if (make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, lda, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        make_map(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, ldb, 128, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+        return FP8BS_EINVAL;
+    if (b_scale_mode == 1 && make_map(&tSB, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sb, N, K / 128, ldsb * 4, BN, 1,
+                                      CU_TENSOR_MAP_SWIZZLE_NONE))
+        return FP8BS_EINVAL;
+    const int64_t tiles = ((M + 127) / 128) * ((N + BN - 1) / BN);
+    const int grid = static_cast<int>(std::min<int64_t>(tiles, d->num_sms));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (b_scale_mode == 0) {
+        if (wide)
+            return out_dtype == 0 ? launch_gemm<256, 4, 0, false, false>(d, 0, tA, tB, tSB, p, grid, st)
+                                  : launch_gemm<256, 4, 0, true, false>(d, 1, tA, tB, tSB, p, grid, st);
+        return out_dtype == 0 ? launch_gemm<128, 6, 0, false, false>(d, 2, tA, tB, tSB, p, grid, st)
+                              : launch_gemm<128, 6, 0, true, false>(d, 3, tA, tB, tSB, p, grid, st);
+    }
+    return out_dtype == 0 ? launch_gemm<128, 6, 1, false, false>(d, 4, tA, tB, tSB, p, grid, st)
+                          : launch_gemm<128, 6, 1, true, false>(d, 5, tA, tB, tSB, p, grid, st);
+}
+
+int fp8_grouped_gemm_moe(const uint8_t *A, int64_t lda, const float *sa, int64_t ldsa, const uint8_t *B,
+                         const float *sb, const int32_t *group_offsets, int G, int64_t M_total, void *C, int64_t ldc,
+                         int out_dtype, int64_t N, int64_t K, void *stream)
+{
+    if (G < 1 || G > gemm::kMaxGroups || !group_offsets)
+        return FP8BS_EINVAL;
+    int rc = gemm_common_checks(A, lda, sa, ldsa, B, sb, C, ldc, out_dtype, M_total, N, K);
+    if (rc < 0)
+        return rc;
+    if (rc == 1)
+        return FP8BS_OK;
+    if (int64_t(G) * N >= (int64_t(1) << 31))
+        return FP8BS_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(group_offsets) & 3))
+        return FP8BS_EALIGN;
+    DeviceInfo *d;
+    rc = current_device(&d);
+    if (rc != FP8BS_OK)
+        return rc;
+
+    gemm::Params p;
+    p.sa = sa;
+    p.ldsa = ldsa;
+    p.sb = sb;
+    p.ldsb = K / 128;
+    p.sb_estride = ((N + 127) / 128) * (K / 128);
+    p.C = C;
+    p.ldc = ldc;
+    p.M = static_cast<int>(M_total);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.offs = group_offsets;
+    p.G = G;
+
+    const bool wide = N > 128;
+    const int BN = wide ? 256 : 128;
+    CUtensorMap tA, tB, tSB;
+    std::memset(&tSB, 0, sizeof tSB);
+    if (make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M_total, lda, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        make_map(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, int64_t(G) * N, K, 128, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+        return FP8BS_EINVAL;
+    // upper bound on the tile count without reading the offsets on the host
+    const int64_t max_tiles = ((M_total + 127) / 128 + G) * ((N + BN - 1) / BN);
+    const int grid = static_cast<int>(std::min<int64_t>(max_tiles, d->num_sms));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (wide)
+        return out_dtype == 0 ? launch_gemm<256, 4, 0, false, true>(d, 6, tA, tB, tSB, p, grid, st)
+                              : launch_gemm<256, 4, 0, true, true>(d, 7, tA, tB, tSB, p, grid, st);
+    return out_dtype == 0 ? launch_gemm<128, 6, 0, false, true>(d, 8, tA, tB, tSB, p, grid, st)
+                          : launch_gemm<128, 6, 0, true, true>(d, 9, tA, tB, tSB, p, grid, st);
+}
+
+int fp8bs_e4m3_encode(const float *x, uint8_t *q, int64_t n, void *stream)
+{
+    if (n < 0)
+        return FP8BS_EINVAL;
+    if (n == 0)
+        return FP8BS_OK;
+    if (!x || !q)
+        return FP8BS_EINVAL;
+    DeviceInfo *d;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK)
+        return rc;
+    const int64_t blocks = std::min<int64_t>((n + 511) / 512, int64_t(d->num_sms) * 8);
+    quant::encode_kernel<<<static_cast<int>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(x, q, n);
+    return launch_status();
+}
+
+int fp8bs_get_device_error(void *stream)
+{
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int h = 0;
+    const int zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&h, g_fp8bs_error, sizeof(int), 0, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_fp8bs_error, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return FP8BS_ECUDA;
+    return h == 0 ? FP8BS_OK : FP8BS_ETIMEOUT;
+}
+
+int fp8bs_selftest_timeout(int64_t timeout_ns, void *stream)
+{
+    if (timeout_ns < 1 || timeout_ns > 1000000000)
+        return FP8BS_EINVAL;
+    DeviceInfo *d;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK)
+        return rc;
+    selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint64_t>(timeout_ns));
+    return launch_status();
+}
+
+}  // extern "C"

@@ -1,0 +1,494 @@
+// gemm.cuh -- block-scaled E4M3 GEMM with FP32 promotion every 128 K, on the
+// sm_103a fifth-generation tensor cores (V3 report §6: FP8 Fprop/Dgrad/Wgrad
+// GEMMs, BF16 or FP32 outputs; §6.2: partial sums promoted to FP32 after
+// every 128 FP8 products).
+//
+// The pages' design promotes on Hopper CUDA cores because the Hopper FP8
+// tensor-core accumulator is short.  Here the promotion is re-shaped for
+// tcgen05: each 128-wide K chunk is one chain of four M128 x BN x K32 MMAs
+// into a fresh FP32 partial in tensor memory (TMEM); promotion warps read the
+// partial with tcgen05.ld and fold it into FP32 register accumulators,
+//     acc[m][n] = fmaf(sa[kb][m] * sb(n, kb), P_kb[m][n], acc[m][n]),
+// while the MMA warp already fills the other TMEM buffer with chunk kb+1.
+//
+// CTA layout (384 threads = 3 warpgroups, one CTA per SM, persistent over
+// output tiles):
+//   warp 0      TMA producer: A and B K-chunks (128 bytes of K per row, the
+//               128-byte swizzle) into a STAGES-deep shared-memory ring.
+//   warp 1      TMEM allocator and MMA issuer (one thread).
+//   warps 2, 3  idle.  Warpgroup 0 gives registers away (setmaxnreg 40).
+//   warps 4..11 promotion + epilogue (setmaxnreg 232: 128 FP32 accumulators
+//               per thread).  Warp w may only read TMEM lanes
+//               32*(w%4) .. 32*(w%4)+31; warps 4..7 cover the left half of the
+//               tile's columns, warps 8..11 the right half.
+//
+// Synchronisation (all mbarriers, all waits bounded):
+//   full[s]   TMA bytes of stage s landed          (producer -> MMA)
+//   empty[s]  MMAs reading stage s are complete    (tcgen05.commit -> producer)
+//   tfull[b]  partial in TMEM buffer b is complete (tcgen05.commit -> promotion)
+//   tempty[b] promotion has read buffer b          (8 warp arrivals -> MMA)
+//   sbfull/sbempty  per-stage B row scales (row-scale mode only)
+#pragma once
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace fp8bs {
+namespace gemm {
+
+constexpr int BM = 128;
+constexpr int BK = 128;
+constexpr int kThreads = 384;
+constexpr int kFirstPromoWarp = 4;
+constexpr int kPromoWarps = 8;
+constexpr int kGroupM = 16;      // raster: 16 M tiles share each sweep over N
+constexpr int kMaxGroups = 1024; // grouped GEMM: experts per call
+
+template <int BN, int STAGES, int BMODE>
+struct Layout {
+    static constexpr int A_BYTES = BM * BK;
+    static constexpr int B_BYTES = BN * BK;
+    static constexpr int SBROW_BYTES = (BMODE == 1) ? BN * 4 : 0;
+    static constexpr int EPI_BYTES = kPromoWarps * 2048;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_SBROW = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_EPI = OFF_SBROW + STAGES * SBROW_BYTES;
+    static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
+    static constexpr int NBAR = 4 * STAGES + 4;
+    static constexpr int OFF_TMEMSLOT = OFF_BAR + NBAR * 8;
+    static constexpr int OFF_TILESTART = (OFF_TMEMSLOT + 4 + 15) / 16 * 16;
+    static constexpr int BYTES = OFF_TILESTART + (kMaxGroups + 1) * 4;
+    static constexpr int ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
+    static constexpr int TMEM_COLS = 2 * BN;    // double-buffered FP32 partials
+    static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
+};
+
+struct Params {
+    const float *sa;
+    int64_t ldsa;
+    const float *sb;     // BMODE 0: sb[nb*ldsb + kb] (per expert: + e*sb_estride)
+    int64_t ldsb;
+    int64_t sb_estride;
+    void *C;
+    int64_t ldc;
+    int M, N, K;         // M = rows of A (M_total when grouped)
+    const int32_t *offs; // grouped: [G+1] row offsets (device)
+    int G;
+};
+
+struct Tile {
+    int m0, m_end, n0, brow0;
+    const float *sbp;    // block scales of this tile's B (BMODE 0)
+    bool valid;
+};
+
+template <int BN, bool GROUPED>
+__device__ __forceinline__ Tile tile_of(int t, const Params &p, const int *tile_start)
+{
+    Tile r;
+    const int num_n = (p.N + BN - 1) / BN;
+    if constexpr (!GROUPED) {
+        const int num_m = (p.M + BM - 1) / BM;
+        const int per_group = kGroupM * num_n;
+        const int g = t / per_group;
+        const int first_m = g * kGroupM;
+        const int gsize = min(num_m - first_m, kGroupM);
+        const int local = t - g * per_group;
+        const int mt = first_m + local % gsize;
+        const int nt = local / gsize;
+        r.m0 = mt * BM;
+        r.m_end = p.M;
+        r.n0 = nt * BN;
+        r.brow0 = r.n0;
+        r.sbp = p.sb;
+        r.valid = true;
+    } else {
+        int lo = 0, hi = p.G;  // largest e with tile_start[e] <= t
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (tile_start[mid] <= t)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const int e = lo;
+        const int base = p.offs[e];
+        const int m_e = p.offs[e + 1] - base;
+        const int mtiles = (m_e + BM - 1) / BM;
+        const int local = t - tile_start[e];
+        const int nt = local / mtiles;
+        const int mt = local - nt * mtiles;
+        r.m0 = base + mt * BM;
+        r.m_end = base + m_e;
+        r.n0 = nt * BN;
+        r.brow0 = e * p.N + r.n0;
+        r.sbp = p.sb + static_cast<int64_t>(e) * p.sb_estride;
+        r.valid = true;
+    }
+    return r;
+}
+
+// Prefix sum of per-expert tile counts, computed by the promotion warps.
+// Malformed ranges (negative length or past M) count as empty.
+template <int BN>
+__device__ void build_tile_start(const Params &p, int *tile_start, int ptid)
+{
+    const int num_n = (p.N + BN - 1) / BN;
+    __shared__ int warp_sums[kPromoWarps];
+    // each promotion thread owns up to 4 consecutive experts
+    constexpr int PER = (kMaxGroups + kPromoWarps * 32 - 1) / (kPromoWarps * 32);
+    int cnt[PER];
+    int local = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int e = ptid * PER + i;
+        int c = 0;
+        if (e < p.G) {
+            const int a = p.offs[e], b = p.offs[e + 1];
+            const int m_e = b - a;
+            if (a >= 0 && m_e > 0 && b <= p.M)
+                c = ((m_e + BM - 1) / BM) * num_n;
+        }
+        cnt[i] = c;
+        local += c;
+    }
+    const int lane = ptid & 31, w = ptid >> 5;
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o)
+            incl += v;
+    }
+    if (lane == 31)
+        warp_sums[w] = incl;
+    asm volatile("bar.sync 1, %0;" ::"n"(kPromoWarps * 32));
+    int before = 0;
+    for (int i = 0; i < w; ++i)
+        before += warp_sums[i];
+    int run = before + incl - local;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int e = ptid * PER + i;
+        if (e < p.G)
+            tile_start[e] = run;
+        run += cnt[i];
+    }
+    if (ptid == kPromoWarps * 32 - 1)
+        tile_start[p.G] = run;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Wait for the registers of the last tcgen05.ld and tie them to the wait so
+// that no use of them is scheduled before it.
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+                   "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]),
+                   "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]),
+                   "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]),
+                   "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+template <int BN, int STAGES, int BMODE, bool OUT_F32, bool GROUPED>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmSB, const Params p)
+{
+    using L = Layout<BN, STAGES, BMODE>;
+    extern __shared__ uint8_t dyn_smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(dyn_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    uint32_t bar_full = sbase + L::OFF_BAR;
+    uint32_t bar_empty = bar_full + 8 * STAGES;
+    uint32_t bar_sbfull = bar_empty + 8 * STAGES;
+    uint32_t bar_sbempty = bar_sbfull + 8 * STAGES;
+    uint32_t bar_tfull = bar_sbempty + 8 * STAGES;
+    uint32_t bar_tempty = bar_tfull + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_TMEMSLOT);
+    int *tile_start = reinterpret_cast<int *>(smem + L::OFF_TILESTART);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+            mbar_init(bar_sbfull + 8 * s, 1);
+            mbar_init(bar_sbempty + 8 * s, kPromoWarps);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_tfull + 8 * b, 1);
+            mbar_init(bar_tempty + 8 * b, kPromoWarps);
+        }
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        if constexpr (BMODE == 1)
+            tma_prefetch_desc(&tmSB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if constexpr (GROUPED) {
+        if (warp >= kFirstPromoWarp)
+            build_tile_start<BN>(p, tile_start, threadIdx.x - kFirstPromoWarp * 32);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int num_kb = p.K / BK;
+    int total_tiles;
+    if constexpr (GROUPED)
+        total_tiles = tile_start[p.G];
+    else
+        total_tiles = ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
+
+    if (warp < kFirstPromoWarp) {
+        regs_dec<40>();
+        if (warp == 0 && lane == 0) {
+            // -------------------------------------------------------- TMA producer
+            uint32_t c = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+                const Tile tl = tile_of<BN, GROUPED>(t, p, tile_start);
+                for (int kb = 0; kb < num_kb; ++kb, ++c) {
+                    const int s = c % STAGES;
+                    const uint32_t ph = (c / STAGES) & 1;
+                    if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, ERR_TIMEOUT_PRODUCER)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar_full + 8 * s, L::A_BYTES + L::B_BYTES);
+                    tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmA, kb * BK, tl.m0, bar_full + 8 * s);
+                    tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, kb * BK, tl.brow0, bar_full + 8 * s);
+                    if constexpr (BMODE == 1) {
+                        if (!mbar_wait(bar_sbempty + 8 * s, ph ^ 1, ERR_TIMEOUT_PRODUCER)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(bar_sbfull + 8 * s, L::SBROW_BYTES);
+                        tma_load_2d(sbase + L::OFF_SBROW + s * L::SBROW_BYTES, &tmSB, tl.n0, kb,
+                                    bar_sbfull + 8 * s);
+                    }
+                }
+            }
+            if (!ok) {
+                // let copies already issued land before the CTA exits
+                const uint32_t issued = c;
+                for (uint32_t d = (issued > STAGES ? issued - STAGES : 0); d < issued; ++d)
+                    mbar_wait(bar_full + 8 * (d % STAGES), (d / STAGES) & 1, ERR_TIMEOUT_PRODUCER, 100000000ull);
+            }
+        } else if (warp == 1 && lane == 0) {
+            // -------------------------------------------------------- MMA issuer
+            constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+            uint32_t c = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+                for (int kb = 0; kb < num_kb; ++kb, ++c) {
+                    const int s = c % STAGES;
+                    const uint32_t ph = (c / STAGES) & 1;
+                    const int b = c & 1;
+                    const uint32_t tph = (c >> 1) & 1;
+                    if (!mbar_wait(bar_tempty + 8 * b, tph ^ 1, ERR_TIMEOUT_MMA) ||
+                        !mbar_wait(bar_full + 8 * s, ph, ERR_TIMEOUT_MMA)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t adesc = sdesc_k128_sw128(sbase + L::OFF_A + s * L::A_BYTES);
+                    const uint64_t bdesc = sdesc_k128_sw128(sbase + L::OFF_B + s * L::B_BYTES);
+                    const uint32_t d_tmem = tmem_base + b * BN;
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k)  // +32 bytes of K = +2 in the address field
+                        mma_f8(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
+                    mma_commit(bar_empty + 8 * s);
+                    mma_commit(bar_tfull + 8 * b);
+                }
+            }
+            if (!ok && c > 0) {
+                // wait for the last committed chain before TMEM is released
+                const uint32_t d = c - 1;
+                mbar_wait(bar_tfull + 8 * (d & 1), (d >> 1) & 1, ERR_TIMEOUT_MMA, 100000000ull);
+            }
+        }
+    } else {
+        regs_inc<232>();
+        // ------------------------------------------------------------ promotion + epilogue
+        const int pw = warp - kFirstPromoWarp;
+        const int quarter = warp & 3;
+        const int half = pw >> 2;
+        constexpr int HALF = BN / 2;  // columns per thread
+        constexpr int NP = HALF / 32; // 32-column pieces
+        const int row = quarter * 32 + lane;
+        const int col0 = half * HALF;
+        const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
+        uint8_t *epi = smem + L::OFF_EPI + pw * 2048;
+        const float *sbrow_smem = reinterpret_cast<const float *>(smem + L::OFF_SBROW);
+
+        uint32_t c = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+            const Tile tl = tile_of<BN, GROUPED>(t, p, tile_start);
+            const int m_row = min(tl.m0 + row, p.M - 1);
+            const float *sa_ptr = p.sa + m_row;
+            int nb = (tl.n0 + col0) / 128;
+            nb = min(nb, (p.N - 1) / 128);
+            const float *sb_ptr = tl.sbp + static_cast<int64_t>(nb) * p.ldsb;
+
+            float acc[HALF];
+#pragma unroll
+            for (int j = 0; j < HALF; ++j)
+                acc[j] = 0.0f;
+
+            float sa_next = __ldg(sa_ptr);
+            float sb_next = (BMODE == 0) ? __ldg(sb_ptr) : 0.0f;
+            for (int kb = 0; kb < num_kb; ++kb, ++c) {
+                const float sa_v = sa_next;
+                const float sb_v = sb_next;
+                if (kb + 1 < num_kb) {
+                    sa_next = __ldg(sa_ptr + static_cast<int64_t>(kb + 1) * p.ldsa);
+                    if constexpr (BMODE == 0)
+                        sb_next = __ldg(sb_ptr + kb + 1);
+                }
+                const int b = c & 1;
+                const uint32_t tph = (c >> 1) & 1;
+                const int s = c % STAGES;
+                // every lane waits, then the warp reconverges before the
+                // .sync.aligned TMEM loads
+                bool got = mbar_wait(bar_tfull + 8 * b, tph, ERR_TIMEOUT_CONSUMER);
+                if constexpr (BMODE == 1)
+                    got = got && mbar_wait(bar_sbfull + 8 * s, (c / STAGES) & 1, ERR_TIMEOUT_CONSUMER);
+                if (!__all_sync(0xFFFFFFFFu, got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + t_lane + b * BN + col0;
+                const float sc = sa_v * sb_v;
+                const float *sbr = sbrow_smem + s * BN + col0;
+                (void)sbr;
+
+                uint32_t ra[32], rb[32];
+                tmem_ld32(taddr, ra);
+                tmem_ld_wait_regs(ra);
+                if constexpr (NP == 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(bar_tempty + 8 * b);
+                }
+#pragma unroll
+                for (int pc = 0; pc < NP; ++pc) {
+                    uint32_t(&cur)[32] = (pc & 1) ? rb : ra;
+                    uint32_t(&nxt)[32] = (pc & 1) ? ra : rb;
+                    if (pc + 1 < NP)
+                        tmem_ld32(taddr + (pc + 1) * 32, nxt);
+                    if constexpr (BMODE == 0) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            acc[pc * 32 + j] = fmaf(sc, __uint_as_float(cur[j]), acc[pc * 32 + j]);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4) {
+                            const float4 sb4 = *reinterpret_cast<const float4 *>(sbr + pc * 32 + j);
+                            acc[pc * 32 + j + 0] = fmaf(sa_v * sb4.x, __uint_as_float(cur[j + 0]), acc[pc * 32 + j + 0]);
+                            acc[pc * 32 + j + 1] = fmaf(sa_v * sb4.y, __uint_as_float(cur[j + 1]), acc[pc * 32 + j + 1]);
+                            acc[pc * 32 + j + 2] = fmaf(sa_v * sb4.z, __uint_as_float(cur[j + 2]), acc[pc * 32 + j + 2]);
+                            acc[pc * 32 + j + 3] = fmaf(sa_v * sb4.w, __uint_as_float(cur[j + 3]), acc[pc * 32 + j + 3]);
+                        }
+                    }
+                    if (pc + 1 < NP) {
+                        tmem_ld_wait_regs(nxt);
+                        if (pc + 2 == NP) {
+                            // the last piece is in registers: release the TMEM buffer
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0)
+                                mbar_arrive(bar_tempty + 8 * b);
+                        }
+                    }
+                }
+                if constexpr (BMODE == 1) {
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(bar_sbempty + 8 * s);
+                }
+            }
+            if (!ok)
+                break;
+
+            // ---------------------------------------------------------- epilogue
+            // Each round stages 32 rows x 64 bytes through this warp's 2 KB
+            // buffer (16-byte chunks XOR-swizzled by row pair, so that the
+            // row-wise writes and the row-contiguous read-back are both free
+            // of bank conflicts), then stores with row/column masks.
+            const int grow0 = tl.m0 + quarter * 32;
+            constexpr int COLS_PER_ROUND = OUT_F32 ? 16 : 32;
+            constexpr int ELEMS_PER_CHUNK = OUT_F32 ? 4 : 8;
+#pragma unroll
+            for (int g = 0; g < HALF / COLS_PER_ROUND; ++g) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float *a = &acc[g * COLS_PER_ROUND + j * ELEMS_PER_CHUNK];
+                    uint4 v;
+                    if constexpr (OUT_F32) {
+                        v = make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                                       __float_as_uint(a[3]));
+                    } else {
+                        v = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                                       pack_bf16x2(a[6], a[7]));
+                    }
+                    *reinterpret_cast<uint4 *>(epi + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)) = v;
+                }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int idx = lane + 32 * i;
+                    const int r = idx >> 2, j = idx & 3;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(epi + r * 64 + ((j ^ ((r >> 1) & 3)) * 16));
+                    const int m = grow0 + r;
+                    const int n = tl.n0 + col0 + g * COLS_PER_ROUND + j * ELEMS_PER_CHUNK;
+                    if (m < tl.m_end && n < p.N) {
+                        const int64_t off = static_cast<int64_t>(m) * p.ldc + n;
+                        if constexpr (OUT_F32)
+                            *reinterpret_cast<uint4 *>(reinterpret_cast<float *>(p.C) + off) = v;
+                        else
+                            *reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.C) + off) = v;
+                    }
+                }
+                __syncwarp();
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, L::TMEM_COLS);
+    }
+}
+
+}  // namespace gemm
+}  // namespace fp8bs

@@ -1,0 +1,277 @@
+// quant.cuh -- BF16 -> E4M3 tile quantisers (V3 report §6.1: 1x128 tiles
+// for activations, 128x128 blocks for weights, scales computed online).
+//
+// Every kernel reads BF16 with 16-byte loads, takes the tile amax on the
+// sign-cleared BF16 bit patterns (for finite inputs their unsigned order is
+// the order of magnitudes, so the maximum is exact), forms the scale
+// amax / 448 with an IEEE single-precision divide (1.0 for an all-zero tile)
+// and each code as E4M3_RNE_sat(x / scale), again with an IEEE divide.
+// All grids are persistent: a CTA walks tiles with a stride of gridDim.x.
+#pragma once
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace fp8bs {
+namespace quant {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// max of the magnitudes held in a 16-byte group of 8 BF16 values, as a pair
+// of 16-bit lanes (sign bits cleared).
+__device__ __forceinline__ uint32_t amax8(const uint4 &v)
+{
+    uint32_t a = __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
+    uint32_t b = __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu);
+    return __vmaxu2(a, b);
+}
+
+__device__ __forceinline__ float pair_max_to_f32(uint32_t m2)
+{
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+    return __uint_as_float(m << 16);
+}
+
+__device__ __forceinline__ float tile_scale(float amax)
+{
+    return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+}
+
+// 8 BF16 values -> 8 codes (two 32-bit words, element j in byte j).
+__device__ __forceinline__ uint2 encode8(const uint4 &v, float s)
+{
+    uint2 r;
+    r.x = e4m3x2(__fdiv_rn(bf16lo(v.x), s), __fdiv_rn(bf16hi(v.x), s)) |
+          (e4m3x2(__fdiv_rn(bf16lo(v.y), s), __fdiv_rn(bf16hi(v.y), s)) << 16);
+    r.y = e4m3x2(__fdiv_rn(bf16lo(v.z), s), __fdiv_rn(bf16hi(v.z), s)) |
+          (e4m3x2(__fdiv_rn(bf16lo(v.w), s), __fdiv_rn(bf16hi(v.w), s)) << 16);
+    return r;
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// Tiles of 128 rows x 128 contiguous columns (one K chunk).  Thread t owns the
+// 16-byte column group t % 16 of rows t/16 + 16p (p = 0..7): eight loads in
+// flight per thread.
+//   kBlock = false: one scale per row per chunk (1x128 tiles), reduced over
+//                   the 16 lanes that share a row; s[kb*lds + m].
+//   kBlock = true : one scale per 128x128 block, reduced over the CTA;
+//                   s[mb*lds + kb].
+// Tile order: kb fastest, so neighbouring CTAs read neighbouring columns.
+// ---------------------------------------------------------------------------
+template <bool kBlock>
+__global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t *__restrict__ x, int64_t M,
+                                                              int64_t K, int64_t ldx,
+                                                              uint8_t *__restrict__ q, int64_t ldq,
+                                                              float *__restrict__ s, int64_t lds)
+{
+    __shared__ uint32_t red[kThreads / 32];
+    const int tid = threadIdx.x;
+    const int c16 = tid & 15;
+    const int r0 = tid >> 4;
+    const int64_t nkb = K / 128;
+    const int64_t ntiles = ((M + 127) / 128) * nkb;
+
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int64_t kb = tile % nkb;
+        const int64_t m0 = (tile / nkb) * 128;
+        const int64_t col = kb * 128 + c16 * 8;
+
+        uint4 v[8];
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            const int64_t m = m0 + r0 + 16 * p;
+            if (m < M)
+                v[p] = ldg_stream(x + m * ldx + col);
+            else
+                v[p] = make_uint4(0, 0, 0, 0);
+        }
+
+        if constexpr (!kBlock) {
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                uint32_t a = amax8(v[p]);
+                a = __vmaxu2(a, __shfl_xor_sync(0xFFFFFFFFu, a, 8));
+                a = __vmaxu2(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
+                a = __vmaxu2(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+                a = __vmaxu2(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+                const float sc = tile_scale(pair_max_to_f32(a));
+                const int64_t m = m0 + r0 + 16 * p;
+                if (m < M) {
+                    *reinterpret_cast<uint2 *>(q + m * ldq + col) = encode8(v[p], sc);
+                    if (c16 == 0)
+                        s[kb * lds + m] = sc;
+                }
+            }
+        } else {
+            uint32_t a = amax8(v[0]);
+#pragma unroll
+            for (int p = 1; p < 8; ++p)
+                a = __vmaxu2(a, amax8(v[p]));
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1)
+                a = __vmaxu2(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+            if ((tid & 31) == 0)
+                red[tid >> 5] = a;
+            __syncthreads();
+            uint32_t b = red[0];
+#pragma unroll
+            for (int w = 1; w < kThreads / 32; ++w)
+                b = __vmaxu2(b, red[w]);
+            const float sc = tile_scale(pair_max_to_f32(b));
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                const int64_t m = m0 + r0 + 16 * p;
+                if (m < M)
+                    *reinterpret_cast<uint2 *>(q + m * ldq + col) = encode8(v[p], sc);
+            }
+            if (tid == 0)
+                s[(m0 / 128) * lds + kb] = sc;
+            __syncthreads();  // red[] is rewritten by the next tile
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Tiles of 128 consecutive rows of one column (the token dimension of a
+// weight-gradient operand), codes written transposed.  A CTA stages a
+// 128-row x 128-column BF16 tile in shared memory (row pitch 65 words: the
+// column reads of 32 consecutive rows hit 32 distinct banks), reduces each
+// column, encodes into a [128 columns][128 rows] byte tile and writes it out
+// with 16-byte coalesced stores.
+//   x [T][ldx] (C columns); q [C][ldq] (row k holds the T codes of column k);
+//   s [T/128][lds]: scale of tile (tb, k) at s[tb*lds + k].
+// ---------------------------------------------------------------------------
+constexpr int kColsPitch = 65;  // words per staged row (64 data words + 1)
+
+struct ColsSmem {
+    uint32_t xs[128 * kColsPitch];
+    uint8_t qs[128 * 128];
+    uint32_t red[4][64];
+    float sc[128];
+};
+
+__global__ void __launch_bounds__(kThreads) quant_cols_kernel(const uint16_t *__restrict__ x, int64_t T,
+                                                              int64_t C, int64_t ldx,
+                                                              uint8_t *__restrict__ q, int64_t ldq,
+                                                              float *__restrict__ s, int64_t lds)
+{
+    extern __shared__ __align__(16) uint8_t dyn_smem[];
+    ColsSmem &sm = *reinterpret_cast<ColsSmem *>(dyn_smem);
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int64_t ntb = T / 128;
+    const int64_t ncb = (C + 127) / 128;
+    const int64_t ntiles = ntb * ncb;
+
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int64_t cb = tile % ncb;
+        const int64_t tb = tile / ncb;
+        const int64_t t0 = tb * 128, c0 = cb * 128;
+
+        // 1. load 128 rows x 256 bytes, 16 bytes per thread per row
+        {
+            const int c16 = tid & 15;
+            const int rr = tid >> 4;
+            uint4 v[8];
+            const bool colok = c0 + c16 * 8 < C;
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                const int64_t t = t0 + rr + 16 * p;
+                v[p] = colok ? ldg_stream(x + t * ldx + c0 + c16 * 8) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                uint32_t *dst = &sm.xs[(rr + 16 * p) * kColsPitch + c16 * 4];
+                dst[0] = v[p].x;
+                dst[1] = v[p].y;
+                dst[2] = v[p].z;
+                dst[3] = v[p].w;
+            }
+        }
+        __syncthreads();
+
+        // 2. column amax: thread -> word column w (2 columns), quarter of the rows
+        {
+            const int w = tid & 63;
+            const int qr = tid >> 6;
+            uint32_t a = 0;
+#pragma unroll 8
+            for (int r = 0; r < 32; ++r)
+                a = __vmaxu2(a, sm.xs[(qr * 32 + r) * kColsPitch + w] & 0x7FFF7FFFu);
+            sm.red[qr][w] = a;
+        }
+        __syncthreads();
+        if (tid < 64) {
+            uint32_t a = __vmaxu2(__vmaxu2(sm.red[0][tid], sm.red[1][tid]),
+                                  __vmaxu2(sm.red[2][tid], sm.red[3][tid]));
+            const float slo = tile_scale(__uint_as_float((a & 0xFFFFu) << 16));
+            const float shi = tile_scale(__uint_as_float(a & 0xFFFF0000u));
+            sm.sc[2 * tid] = slo;
+            sm.sc[2 * tid + 1] = shi;
+            if (c0 + 2 * tid < C) {
+                s[tb * lds + c0 + 2 * tid] = slo;
+                s[tb * lds + c0 + 2 * tid + 1] = shi;
+            }
+        }
+        __syncthreads();
+
+        // 3. encode: warp -> 8 word columns; lane -> rows lane + 32j
+#pragma unroll 1
+        for (int i = 0; i < 8; ++i) {
+            const int w = warp * 8 + i;
+            const float slo = sm.sc[2 * w], shi = sm.sc[2 * w + 1];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int r = lane + 32 * j;
+                const uint32_t word = sm.xs[r * kColsPitch + w];
+                const uint32_t c2 = e4m3x2(__fdiv_rn(bf16lo(word), slo), __fdiv_rn(bf16hi(word), shi));
+                sm.qs[(2 * w) * 128 + r] = static_cast<uint8_t>(c2 & 0xFF);
+                sm.qs[(2 * w + 1) * 128 + r] = static_cast<uint8_t>(c2 >> 8);
+            }
+        }
+        __syncthreads();
+
+        // 4. write the transposed code tile: 128 rows x 8 chunks of 16 bytes
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int idx = tid + kThreads * i;
+            const int row = idx >> 3, ch = idx & 7;
+            if (c0 + row < C) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(&sm.qs[row * 128 + ch * 16]);
+                *reinterpret_cast<uint4 *>(q + (c0 + row) * ldq + t0 + ch * 16) = v;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// Element-wise conversion with the quantisers' E4M3 rounding (diagnostic).
+__global__ void encode_kernel(const float *__restrict__ x, uint8_t *__restrict__ q, int64_t n)
+{
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * 2;
+    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 2; i < n; i += stride) {
+        if (i + 1 < n) {
+            const uint32_t c = e4m3x2(x[i], x[i + 1]);
+            q[i] = static_cast<uint8_t>(c & 0xFF);
+            q[i + 1] = static_cast<uint8_t>(c >> 8);
+        } else {
+            q[i] = static_cast<uint8_t>(e4m3x2(x[i], 0.0f) & 0xFF);
+        }
+    }
+}
+
+}  // namespace quant
+}  // namespace fp8bs

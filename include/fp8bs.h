@@ -1,0 +1,163 @@
+/*
+ * fp8bs.h -- C ABI of libfp8bs: fine-grained FP8 (E4M3) quantisation and
+ * block-scaled GEMM with FP32 promotion, for NVIDIA B300 (sm_103a).
+ *
+ * Method (web pages on DeepSeek-V3):
+ *   "DeepSeek-V3 技术报告：从 671B MoE 到低成本训练系统" (xutianle.me):
+ *     §6   the Fprop, Dgrad and Wgrad GEMMs of every Linear take FP8 inputs;
+ *          their outputs stay in BF16 or FP32.
+ *     §6.1 activations are scaled per 1x128 tile (one scale per token per 128
+ *          channels), weights per 128x128 block, scales computed online.
+ *     §6.2 after every 128 FP8 products the tensor-core partial sum is
+ *          promoted and accumulated in FP32.
+ *     §2   DeepSeekMoE: 256 routed experts, 8 chosen per token.
+ *   51itzy.com infra commentary on DeepSeek-V3, FP8 paragraph: E4M3 in both
+ *     the forward and the backward pass.
+ * Readings where the pages are silent: OCP E4M3FN (max 448); scale =
+ * amax / 448 as an IEEE FP32 divide (1.0 for an all-zero tile); code =
+ * E4M3(x / scale) with an IEEE FP32 divide, round-to-nearest-even, saturating
+ * at +-448, sign kept.
+ *
+ * Conventions for every call:
+ *   - All pointers are DEVICE pointers owned by the caller, except where a
+ *     parameter says otherwise.  The library allocates no device memory per
+ *     call.  `stream` is a cudaStream_t (NULL = legacy default stream).
+ *   - Calls are asynchronous on `stream`; the library never synchronises,
+ *     except fp8bs_get_device_error.
+ *   - Argument errors are returned synchronously before any launch.  A failed
+ *     launch returns FP8BS_ECUDA.  A kernel that gives up on a bounded
+ *     internal wait records FP8BS_ETIMEOUT in a device error word read by
+ *     fp8bs_get_device_error.
+ *   - Leading dimensions (ld*) are in elements.  Code and BF16/FP32 matrices
+ *     are row-major.  Base pointers must be 16-byte aligned and every row
+ *     pitch a multiple of 16 bytes (FP8BS_EALIGN otherwise).
+ *   - The device must be sm_103 (FP8BS_EARCH otherwise).
+ */
+#ifndef FP8BS_H
+#define FP8BS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8BS_OK = 0,
+    FP8BS_EINVAL = -1,   /* bad size, mode or null pointer */
+    FP8BS_EALIGN = -2,   /* pointer or pitch not 16-byte aligned */
+    FP8BS_EARCH = -3,    /* current device is not sm_103 */
+    FP8BS_ECUDA = -4,    /* CUDA runtime/driver error at launch */
+    FP8BS_ETIMEOUT = -5  /* a kernel gave up on a bounded wait */
+} fp8bs_status;
+
+/*
+ * fp8_quant_1x128 -- per-tile 1x128 quantisation of a BF16 matrix
+ * (V3 report §6.1: one scale per token per 128 channels; E4M3, online scale).
+ *
+ *   x      BF16 [M][ldx], K columns used.
+ *   along  0: tiles run along the contiguous dimension: tile (m, kb) is
+ *             x[m][128kb .. 128kb+127].
+ *             q = codes [M][ldq] (ldq >= K); s = FP32 [K/128][lds], lds >= M
+ *             (scale of tile (m, kb) at s[kb*lds + m]).
+ *          1: tiles run along rows (used for the weight-gradient GEMM, whose
+ *             reduction runs over tokens): tile (tb, k) is x[128tb .. 128tb+127][k].
+ *             The codes come out transposed so that rows are contiguous:
+ *             q = codes [K][ldq] (ldq >= M), q[k*ldq + m];
+ *             s = FP32 [M/128][lds], lds >= K (scale of tile (tb, k) at s[tb*lds + k]).
+ *   Requires K % 128 == 0 (along 0) or M % 128 == 0 (along 1), M, K > 0 or
+ *   an empty matrix (M == 0 or K == 0 returns FP8BS_OK without a launch).
+ *   Codes are uint8 E4M3 bit patterns.  Bit-exact with the reading above.
+ */
+int fp8_quant_1x128(const void *x, int64_t M, int64_t K, int64_t ldx, int along,
+                    uint8_t *q, int64_t ldq, float *s, int64_t lds, void *stream);
+
+/*
+ * fp8_quant_128x128 -- per-block 128x128 quantisation of a BF16 weight
+ * matrix (V3 report §6.1).
+ *   w  BF16 [N][ldw], K columns used; q = codes [N][ldq];
+ *   s  FP32 [ceil(N/128)][lds], lds >= K/128: scale of block (nb, kb) at
+ *      s[nb*lds + kb].  A partial last block row (N % 128 != 0) takes its
+ *      amax over the rows that exist.
+ *   Requires K % 128 == 0.
+ */
+int fp8_quant_128x128(const void *w, int64_t N, int64_t K, int64_t ldw,
+                      uint8_t *q, int64_t ldq, float *s, int64_t lds, void *stream);
+
+/*
+ * fp8_gemm_blockscaled -- C = A * B^T from E4M3 codes with fine-grained
+ * scales and FP32 promotion every 128 K (V3 report §6, §6.2).
+ *
+ *   A   codes [M][lda], K used;   sa FP32 [K/128][ldsa], ldsa >= M.
+ *   B   codes [N][ldb], K used.
+ *   b_scale_mode 0: sb FP32 [ceil(N/128)][ldsb], ldsb >= K/128: one scale per
+ *                   128x128 block of B (weights; Fprop and Dgrad).
+ *                1: sb FP32 [K/128][ldsb], ldsb >= N, ldsb % 4 == 0: one scale
+ *                   per row of B per 128 K (both operands tiled 1x128 along
+ *                   K, as in the weight-gradient GEMM).
+ *   C   [M][ldc]; out_dtype 0: BF16 (round to nearest even), 1: FP32.
+ *   Result: for each 128-wide K chunk kb the tensor cores form the FP32
+ *   partial P_kb of the E4M3 products, and
+ *       C[m][n] = sum_kb  fl32(sa[kb][m] * sb(n, kb)) * P_kb[m][n]
+ *   accumulated in FP32 (fused multiply-add), in order of kb.
+ *   Requires K % 128 == 0, N % 8 == 0, M, N >= 0 (empty -> no launch).
+ */
+int fp8_gemm_blockscaled(const uint8_t *A, int64_t lda, const float *sa, int64_t ldsa,
+                         const uint8_t *B, int64_t ldb, const float *sb, int64_t ldsb,
+                         int b_scale_mode, void *C, int64_t ldc, int out_dtype,
+                         int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
+ * fp8_grouped_gemm_moe -- per-expert block-scaled GEMMs over expert-sorted
+ * rows (V3 report §2: routed experts; §6: FP8 GEMMs).
+ *
+ *   A   codes [M_total][lda], rows sorted by expert; sa FP32 [K/128][ldsa],
+ *       ldsa >= M_total.
+ *   B   codes [G][N][K] (contiguous); sb FP32 [G][ceil(N/128)][K/128]
+ *       (contiguous): expert e's weights and 128x128 block scales.
+ *   group_offsets  DEVICE int32 [G+1]: rows offs[e] .. offs[e+1]-1 belong to
+ *       expert e; offs[0] == 0, non-decreasing, offs[G] <= M_total.  The
+ *       offsets are read on the device only (no host synchronisation);
+ *       malformed offsets make the kernel skip the offending experts.
+ *   C   [M_total][ldc], out_dtype as above; rows of empty experts and rows
+ *       past offs[G] are not written.
+ *   Requires K % 128 == 0, N % 8 == 0, 1 <= G <= 1024.
+ */
+int fp8_grouped_gemm_moe(const uint8_t *A, int64_t lda, const float *sa, int64_t ldsa,
+                         const uint8_t *B, const float *sb, const int32_t *group_offsets,
+                         int G, int64_t M_total, void *C, int64_t ldc, int out_dtype,
+                         int64_t N, int64_t K, void *stream);
+
+/*
+ * fp8bs_e4m3_encode -- element-wise q[i] = E4M3_RNE_saturate(x[i]) with the
+ * same conversion the quantisers use; x FP32 [n], q uint8 [n] (device).
+ * A diagnostic for checking the conversion exhaustively.
+ */
+int fp8bs_e4m3_encode(const float *x, uint8_t *q, int64_t n, void *stream);
+
+/* Human-readable text for a status code (static storage). */
+const char *fp8bs_status_string(int status);
+
+/*
+ * fp8bs_get_device_error -- synchronise `stream`, read and clear the device
+ * error word of the current device.  Returns FP8BS_OK, FP8BS_ETIMEOUT (a
+ * kernel abandoned a bounded wait), or FP8BS_ECUDA.
+ */
+int fp8bs_get_device_error(void *stream);
+
+/*
+ * fp8bs_selftest_timeout -- launch one block that waits on a barrier nothing
+ * will complete, with a wait bound of `timeout_ns` nanoseconds (1 .. 1e9),
+ * so that callers can check the timeout path: the kernel records
+ * FP8BS_ETIMEOUT and returns; nothing faults or hangs.
+ */
+int fp8bs_selftest_timeout(int64_t timeout_ns, void *stream);
+
+/* Version string of the library build. */
+const char *fp8bs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BS_H */

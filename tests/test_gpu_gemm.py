@@ -1,0 +1,196 @@
+"""GPU parity: block-scaled GEMM and grouped MoE GEMM against the oracle,
+through the C ABI, within the tolerance stated in tests/gpu_util.py.
+
+Each side quantises the same seeded BF16 inputs with its own quantiser (the
+quantisers are bit-exact, see test_gpu_quant.py) and multiplies its own codes.
+Small cases span several tiles and ragged edges and are checked in full;
+the full-size workloads are checked on seeded row samples (the tolerance is
+per row, so a row sample checks it exactly for those rows)."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from tests.gpu_util import assert_gemm_close, dev, host_bits, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fb():
+    import fp8_fine_grained_27_b300 as fb
+    assert torch.cuda.is_available()
+    return fb
+
+
+def _dense(fb, orc, a_bits, w_bits, out_dtype=torch.bfloat16, rows=None, what=""):
+    qa, sa = fb.quant_1x128(dev(a_bits))
+    qb, sb = fb.quant_128x128(dev(w_bits))
+    C = fb.gemm_blockscaled(qa, sa, qb, sb, 0, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert fb.get_device_error() == 0
+    oqa, osa = orc.quant_1x128_rows(a_bits)
+    oqb, osb = orc.quant_128x128(w_bits)
+    if rows is None:
+        rows = np.arange(a_bits.shape[0])
+    ref = orc.gemm_blockscaled(oqa, osa, oqb, osb, 0, rows=rows)
+    got = host_bits(C[torch.from_numpy(rows).cuda()])
+    if out_dtype == torch.bfloat16:
+        ref = orc.bf16_round(ref)
+    return assert_gemm_close(got, ref, what)
+
+
+def test_tiny_workload(fb, orc):
+    d = synth.tiny()
+    _dense(fb, orc, d["A"], d["B"], what="tiny")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 128), (300, 392, 640), (129, 72, 256), (257, 520, 384), (64, 128, 1024)])
+def test_ragged_shapes(fb, orc, M, N, K):
+    a = synth.fill_bf16(synth.OUTLIER, synth.key(80, M), (M, K), 1.0, 0.01, 50.0, k2=synth.key(81, M))
+    w = synth.fill_bf16(synth.NORMAL, synth.key(82, N), (N, K), 0.02)
+    _dense(fb, orc, a, w, what=f"{M}x{N}x{K}")
+    _dense(fb, orc, a, w, out_dtype=torch.float32, what=f"{M}x{N}x{K} fp32")
+
+
+def test_mla_full(fb, orc):
+    """Both MLA down-projections, every output checked."""
+    d = synth.mla()
+    _dense(fb, orc, d["A"], d["Wq"], what="mla q")
+    _dense(fb, orc, d["A"], d["Wkv"], what="mla kv")
+
+
+def test_ffn_sampled_rows(fb, orc):
+    d = synth.ffn()
+    rows = sample_rows(16384, 384, seed=5, must=(0, 127, 128, 16383))
+    _dense(fb, orc, d["A"], d["B"], rows=rows, what="ffn")
+
+
+def _wgrad(fb, orc, dY, X, rows=None, what=""):
+    qdy, sdy = fb.quant_1x128(dev(dY), along=1)   # [Cout, T], [T/128, Cout]
+    qx, sx = fb.quant_1x128(dev(X), along=1)      # [Cin, T],  [T/128, Cin]
+    C = fb.gemm_blockscaled(qdy, sdy, qx, sx, 1, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert fb.get_device_error() == 0
+    oqdy, osdy = orc.quant_1x128_cols(dY)
+    oqx, osx = orc.quant_1x128_cols(X)
+    if rows is None:
+        rows = np.arange(oqdy.shape[0])
+    ref = orc.gemm_blockscaled(oqdy, osdy, oqx, osx, 1, rows=rows)
+    got = host_bits(C[torch.from_numpy(rows).cuda()])
+    return assert_gemm_close(got, ref, what)
+
+
+def test_wgrad_small_full(fb, orc):
+    d = synth.wgrad(T=1024, Cout=256, Cin=392)
+    _wgrad(fb, orc, d["dY"], d["X"], what="wgrad small")
+
+
+def test_wgrad_full_size_sampled(fb, orc):
+    d = synth.wgrad()
+    rows = sample_rows(2048, 96, seed=6, must=(0, 2047))
+    _wgrad(fb, orc, d["dY"], d["X"], rows=rows, what="wgrad")
+
+
+def _grouped(fb, orc, a_bits, offs, w_bits, rows=None, what=""):
+    G, N, K = w_bits.shape
+    qa, sa = fb.quant_1x128(dev(a_bits))
+    wd = dev(w_bits)
+    qb = torch.empty((G, N, K), dtype=torch.uint8, device="cuda")
+    sb = torch.empty((G, (N + 127) // 128, K // 128), dtype=torch.float32, device="cuda")
+    for e in range(G):  # per expert: a 128x128 block never spans two experts
+        fb.quant_128x128(wd[e], q=qb[e], s=sb[e])
+    offs_d = torch.from_numpy(offs.astype(np.int32)).cuda()
+    C = torch.full((a_bits.shape[0], N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    fb.grouped_gemm_moe(qa, sa, qb, sb, offs_d, C=C)
+    torch.cuda.synchronize()
+    assert fb.get_device_error() == 0
+    oqa, osa = orc.quant_1x128_rows(a_bits)
+    oqb = np.empty((G, N, K), np.uint8)
+    osb = np.empty((G, (N + 127) // 128, K // 128), np.float32)
+    for e in range(G):
+        oqb[e], osb[e] = orc.quant_128x128(w_bits[e])
+    M = a_bits.shape[0]
+    if rows is None:
+        rows = np.arange(offs[0], offs[-1])
+    ref = orc.bf16_round(orc.grouped_gemm(oqa, osa, oqb, osb, offs, rows=rows))
+    got = host_bits(C[torch.from_numpy(rows).cuda()])
+    assert_gemm_close(got, ref, what)
+    # rows outside every group are left untouched
+    outside = np.setdiff1d(np.arange(M), np.arange(offs[0], offs[-1]))
+    if outside.size:
+        assert torch.isnan(C[torch.from_numpy(outside).cuda()].float()).all()
+
+
+@pytest.mark.parametrize("N", [256, 136, 64])
+def test_grouped_small_skewed(fb, orc, N):
+    sizes = [0, 5, 0, 128, 129, 1, 300, 0, 64, 256, 0, 0, 77, 2, 0, 31]
+    offs = np.concatenate([[0], np.cumsum(sizes)])
+    M = int(offs[-1]) + 10  # trailing rows belong to no expert
+    K = 384
+    a = synth.fill_bf16(synth.NORMAL, synth.key(70, N), (M, K), 1.0)
+    w = synth.fill_bf16(synth.NORMAL, synth.key(71, N), (len(sizes), N, K), 0.02)
+    _grouped(fb, orc, a, offs, w, what=f"grouped N={N}")
+
+
+def test_grouped_256_experts_routed(fb, orc):
+    """256 experts, top-8 routing of 512 tokens (skewed groups, many empty)."""
+    tok = synth.moe_tokens(T=512, D=256)
+    offs, token_of_row = synth.moe_route(tok, E=256, topk=8)
+    a = np.ascontiguousarray(tok[token_of_row])
+    w = synth.fill_bf16(synth.NORMAL, synth.key(72, 0), (256, 256, 256), 0.02)
+    _grouped(fb, orc, a, offs.astype(np.int64), w, what="grouped 256")
+
+
+def test_moe_full_size_sampled(fb, orc):
+    """Config-3 shapes: 4096 tokens routed top-8 over 256 experts -> 32768 rows;
+    up (N=4096, K=7168) and down (N=7168, K=2048) grouped GEMMs, checked on
+    every row of 12 experts (the largest, the smallest non-empty, and random)."""
+    tok = synth.moe_tokens()
+    offs, token_of_row = synth.moe_route(tok)
+    offs = offs.astype(np.int64)
+    sizes = np.diff(offs)
+    nonempty = np.nonzero(sizes)[0]
+    rng = np.random.default_rng(3)
+    pick = {int(nonempty[np.argmax(sizes[nonempty])]), int(nonempty[np.argmin(sizes[nonempty])])}
+    pick.update(int(e) for e in rng.choice(nonempty, 10, replace=False))
+    pick = sorted(pick)
+    rows = np.concatenate([np.arange(offs[e], offs[e + 1]) for e in pick])
+
+    for which, A_bits in (("up", np.ascontiguousarray(tok[token_of_row])), ("down", synth.moe_down_input())):
+        G = 256
+        qa, sa = fb.quant_1x128(dev(A_bits))
+        N, K = (4096, 7168) if which == "up" else (7168, 2048)
+        qb = torch.empty((G, N, K), dtype=torch.uint8, device="cuda")
+        sb = torch.empty((G, N // 128, K // 128), dtype=torch.float32, device="cuda")
+        for e0 in range(0, G, 16):
+            w = dev(synth.moe_weights(which, e0, e0 + 16))
+            fb.quant_128x128(w.reshape(16 * N, K), q=qb[e0:e0 + 16].view(16 * N, K),
+                             s=sb[e0:e0 + 16].view(16 * N // 128, K // 128))
+            del w
+        C = fb.grouped_gemm_moe(qa, sa, qb, sb, torch.from_numpy(offs.astype(np.int32)).cuda())
+        torch.cuda.synchronize()
+        assert fb.get_device_error() == 0
+        got = host_bits(C[torch.from_numpy(rows).cuda()])
+        del qb, sb, C
+        oqa, osa = orc.quant_1x128_rows(A_bits)
+        ref = np.empty((rows.size, N), np.float32)
+        pos = 0
+        for e in pick:
+            r = np.arange(offs[e], offs[e + 1])
+            oqb, osb = orc.quant_128x128(synth.moe_weights(which, e, e + 1)[0])
+            ref[pos:pos + r.size] = orc.gemm_blockscaled(oqa, osa, oqb, osb, 0, rows=r)
+            pos += r.size
+        assert_gemm_close(got, orc.bf16_round(ref), f"moe {which}")
+
+
+def test_timeout_path_reports_and_recovers(fb):
+    """A wait that nothing completes ends after ~1 ms with FP8BS_ETIMEOUT recorded;
+    the context stays usable and the error word is cleared by the read."""
+    fb.selftest_timeout(1_000_000)
+    assert fb.get_device_error() == fb.binding.ETIMEOUT
+    assert fb.get_device_error() == 0
+    x = torch.ones((128, 128), dtype=torch.bfloat16, device="cuda")
+    q, s = fb.quant_1x128(x)
+    torch.cuda.synchronize()
+    assert int(q[0, 0]) == 0x7E and float(s[0, 0]) == float(np.float32(1) / np.float32(448))

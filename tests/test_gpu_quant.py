@@ -1,0 +1,137 @@
+"""GPU parity: E4M3 conversion and the 1x128 / 128x128 quantisers, bit-exact
+against the oracle (codes and scales), through the C ABI.
+
+Sizes: small ragged cases that span several tiles plus the full tensors of
+every workload (tiny, MLA, MoE sampled experts, Wgrad, FFN)."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from tests.gpu_util import dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fb():
+    import fp8_fine_grained_27_b300 as fb
+    assert torch.cuda.is_available()
+    return fb
+
+
+def _rows(fb, orc, x_bits):
+    q, s = fb.quant_1x128(dev(x_bits))
+    torch.cuda.synchronize()
+    qr, sr = orc.quant_1x128_rows(x_bits)
+    assert np.array_equal(s.cpu().numpy(), sr), "scales differ"
+    bad = np.count_nonzero(q.cpu().numpy() != qr)
+    assert bad == 0, f"{bad} codes differ"
+
+
+def _block(fb, orc, w_bits):
+    q, s = fb.quant_128x128(dev(w_bits))
+    torch.cuda.synchronize()
+    qr, sr = orc.quant_128x128(w_bits)
+    assert np.array_equal(s.cpu().numpy(), sr), "scales differ"
+    bad = np.count_nonzero(q.cpu().numpy() != qr)
+    assert bad == 0, f"{bad} codes differ"
+
+
+def _cols(fb, orc, x_bits):
+    q, s = fb.quant_1x128(dev(x_bits), along=1)
+    torch.cuda.synchronize()
+    qr, sr = orc.quant_1x128_cols(x_bits)
+    assert np.array_equal(s.cpu().numpy(), sr), "scales differ"
+    bad = np.count_nonzero(q.cpu().numpy() != qr)
+    assert bad == 0, f"{bad} codes differ"
+
+
+def test_encode_exhaustive(fb, orc):
+    """Every non-NaN FP32 bit pattern through the kernels' E4M3 conversion."""
+    chunk = 1 << 28
+    for lo in range(0, 1 << 32, chunk):
+        pat = torch.arange(lo, lo + chunk, dtype=torch.int64, device="cuda").to(torch.int32)
+        x = pat.view(torch.float32)
+        q = fb.e4m3_encode(x).cpu().numpy()
+        ref = orc.e4m3_encode_patterns(lo, chunk)
+        xs = np.arange(lo, lo + chunk, dtype=np.uint64).astype(np.uint32).view(np.float32)
+        keep = ~np.isnan(xs)
+        bad = np.count_nonzero(q[keep] != ref[keep])
+        assert bad == 0, f"patterns {lo:#x}..: {bad} codes differ"
+
+
+def test_rows_small_ragged(fb, orc):
+    for (M, K, seed) in [(1, 128, 1), (127, 256, 2), (129, 384, 3), (300, 1024, 4)]:
+        a = synth.fill_bf16(synth.OUTLIER, synth.key(90, seed), (M, K), 1.0, 0.02, 30.0, k2=synth.key(91, seed))
+        _rows(fb, orc, a)
+
+
+def test_rows_wide_dynamic_range(fb, orc):
+    """Tiles whose scales span ~2^-60 .. 2^60, with exact zeros and -0."""
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((256, 2048)).astype(np.float32)
+    x *= np.exp2(rng.integers(-60, 60, (256, 16))).repeat(128, axis=1).astype(np.float32)
+    x[3, :128] = 0.0
+    x[4, 128:256] = -0.0
+    x[5, 256:384] = 1e-38  # subnormal inputs: the tile scale is subnormal too
+    bits = (x.view(np.uint32) >> 16).astype(np.uint16)
+    _rows(fb, orc, bits)
+
+
+def test_rows_tiny_workload(fb, orc):
+    _rows(fb, orc, synth.tiny()["A"])
+
+
+def test_block_small_ragged(fb, orc):
+    for (N, K, seed) in [(1, 128, 1), (200, 256, 2), (576, 512, 3)]:
+        _block(fb, orc, synth.fill_bf16(synth.NORMAL, synth.key(92, seed), (N, K), 0.02))
+
+
+def test_block_tiny_workload(fb, orc):
+    _block(fb, orc, synth.tiny()["B"])
+
+
+def test_mla_full(fb, orc):
+    d = synth.mla()
+    _rows(fb, orc, d["A"])
+    _block(fb, orc, d["Wq"])
+    _block(fb, orc, d["Wkv"])  # 576 rows: last block is 64 rows
+
+
+def test_cols_small_ragged(fb, orc):
+    for (T, C, seed) in [(128, 8, 1), (384, 200, 2), (512, 1032, 3)]:
+        _cols(fb, orc, synth.fill_bf16(synth.NORMAL, synth.key(93, seed), (T, C), 1e-2))
+
+
+def test_wgrad_full(fb, orc):
+    d = synth.wgrad()
+    _cols(fb, orc, d["dY"])
+    _cols(fb, orc, d["X"])
+
+
+def test_ffn_full(fb, orc):
+    d = synth.ffn()
+    _rows(fb, orc, d["A"])
+    _block(fb, orc, d["B"])
+
+
+def test_moe_tokens_and_sampled_experts(fb, orc):
+    _rows(fb, orc, synth.moe_tokens())
+    _rows(fb, orc, synth.moe_down_input())
+    for which in ("up", "down"):
+        for e in (0, 1, 128, 255):
+            w = synth.moe_weights(which, e, e + 1)[0]
+            _block(fb, orc, w)
+
+
+def test_strided_views(fb, orc):
+    """Leading dimensions larger than the used width (16-byte multiples)."""
+    a = synth.fill_bf16(synth.NORMAL, synth.key(94, 0), (200, 520), 1.0)
+    x = dev(a)[:, :384]
+    q = torch.zeros((200, 400), dtype=torch.uint8, device="cuda")[:, :384]
+    s = torch.zeros((3, 208), dtype=torch.float32, device="cuda")[:, :200]
+    fb.quant_1x128(x, q=q, s=s)
+    torch.cuda.synchronize()
+    qr, sr = orc.quant_1x128_rows(np.ascontiguousarray(a[:, :384]))
+    assert np.array_equal(q.cpu().numpy(), qr) and np.array_equal(s.cpu().numpy(), sr)
