@@ -11,7 +11,7 @@ One step = one pass of the whole hot path over one batch of the workload:
         grouped rows, up grouped GEMM (N=4096, K=7168) with pre-quantised
         expert weights.
 Inputs are seeded synthetic tensors (synth/), resident in HBM before timing.
-L2 is flushed (a 512 MB write) before every timed step, outside the step's
+L2 is flushed (a 256 MB write by default) before every timed step, outside the step's
 CUDA events.  Prints one JSON line (rank 0).
 
 --impl reference times the CPU oracle (oracle/) on a bounded sample of the
@@ -242,7 +242,7 @@ def run_ours(args, rank, world):
         dist.init_process_group("nccl")
     step = Step(args.workload, fb, torch, seed=rank)
     launches = step.launches()
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
@@ -312,7 +312,7 @@ def run_ours(args, rank, world):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> fp32 accumulate",
         "data": "synthetic (seeded; shapes of the DeepSeek-V3 pages)",
-        "config": {**workload_desc(args.workload), "l2": "flushed (512 MB write) before every step",
+        "config": {**workload_desc(args.workload), "l2": f"flushed ({args.flush_mb} MB write) before every step",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(fp8_peak, 1),
                      "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4), "traffic": None,
@@ -482,6 +482,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--flush-mb", type=int, default=256, help="L2 flush buffer (> 126 MB L2)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", args.gpus))
