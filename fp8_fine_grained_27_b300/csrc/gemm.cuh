@@ -15,8 +15,12 @@
 // output tiles):
 //   warp 0      TMA producer: A and B K-chunks (128 bytes of K per row, the
 //               128-byte swizzle) into a STAGES-deep shared-memory ring.
-//   warp 1      TMEM allocator and MMA issuer (one thread).
-//   warps 2, 3  idle.  Warpgroup 0 gives registers away (setmaxnreg 40).
+//   warps 1, 3  MMA issuers (one thread each): warp 1 issues the even K
+//               chunks, warp 3 the odd ones.  Issuing a tcgen05.mma costs the
+//               issuing thread about as long as a 128 x 128 x 32 MMA takes to
+//               execute, so two issuers keep the tensor pipe fed; each one
+//               commits its own chunks.  Warp 1 also owns the TMEM allocation.
+//   warp 2      idle.  Warpgroup 0 gives registers away (setmaxnreg 40).
 //   warps 4..11 promotion + epilogue (setmaxnreg 232: 128 FP32 accumulators
 //               per thread).  Warp w may only read TMEM lanes
 //               32*(w%4) .. 32*(w%4)+31; warps 4..7 cover the left half of the
@@ -298,13 +302,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (uint32_t d = (issued > STAGES ? issued - STAGES : 0); d < issued; ++d)
                     mbar_wait(bar_full + 8 * (d % STAGES), (d / STAGES) & 1, ERR_TIMEOUT_PRODUCER, 100000000ull);
             }
-        } else if (warp == 1 && lane == 0) {
-            // -------------------------------------------------------- MMA issuer
+        } else if ((warp == 1 || warp == 3) && lane == 0) {
+            // -------------------------------------------------------- MMA issuers
+            const uint32_t mine = (warp == 1) ? 0u : 1u;  // chunk parity this thread issues
             constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
             uint32_t c = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
                 for (int kb = 0; kb < num_kb; ++kb, ++c) {
+                    if ((c & 1u) != mine)
+                        continue;
                     const int s = c % STAGES;
                     const uint32_t ph = (c / STAGES) & 1;
                     const int b = c & 1;
@@ -325,10 +332,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(bar_tfull + 8 * b);
                 }
             }
-            if (!ok && c > 0) {
-                // wait for the last committed chain before TMEM is released
-                const uint32_t d = c - 1;
-                mbar_wait(bar_tfull + 8 * (d & 1), (d >> 1) & 1, ERR_TIMEOUT_MMA, 100000000ull);
+            if (!ok) {
+                // wait for this thread's last committed chain before TMEM is released
+                uint32_t d = c;
+                while (d > 0 && ((d - 1) & 1u) != mine)
+                    --d;
+                if (d > 0) {
+                    --d;
+                    mbar_wait(bar_tfull + 8 * (d & 1), (d >> 1) & 1, ERR_TIMEOUT_MMA, 100000000ull);
+                }
             }
         }
     } else {
@@ -360,16 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < HALF; ++j)
                 acc[j] = 0.0f;
 
-            float sa_next = __ldg(sa_ptr);
-            float sb_next = (BMODE == 0) ? __ldg(sb_ptr) : 0.0f;
-            for (int kb = 0; kb < num_kb; ++kb, ++c) {
-                const float sa_v = sa_next;
-                const float sb_v = sb_next;
-                if (kb + 1 < num_kb) {
-                    sa_next = __ldg(sa_ptr + static_cast<int64_t>(kb + 1) * p.ldsa);
-                    if constexpr (BMODE == 0)
-                        sb_next = __ldg(sb_ptr + kb + 1);
-                }
+            // One K chunk: wait for its partial, read it from TMEM, release the
+            // buffer, fold it into acc with the chunk's scales.
+            auto promote = [&](float sa_v, float sb_v) -> bool {
                 const int b = c & 1;
                 const uint32_t tph = (c >> 1) & 1;
                 const int s = c % STAGES;
@@ -378,10 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool got = mbar_wait(bar_tfull + 8 * b, tph, ERR_TIMEOUT_CONSUMER);
                 if constexpr (BMODE == 1)
                     got = got && mbar_wait(bar_sbfull + 8 * s, (c / STAGES) & 1, ERR_TIMEOUT_CONSUMER);
-                if (!__all_sync(0xFFFFFFFFu, got)) {
-                    ok = false;
-                    break;
-                }
+                if (!__all_sync(0xFFFFFFFFu, got))
+                    return false;
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + t_lane + b * BN + col0;
                 const float sc = sa_v * sb_v;
@@ -433,7 +436,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0)
                         mbar_arrive(bar_sbempty + 8 * s);
                 }
+                ++c;
+                return true;
+            };
+
+            // Scales are loaded two chunks ahead into two fixed registers per
+            // operand (the chunk loop is unrolled by two), so each load has a
+            // whole chunk pair to land and no register copy waits on it.
+            auto ld_sa = [&](int kb) { return kb < num_kb ? __ldg(sa_ptr + static_cast<int64_t>(kb) * p.ldsa) : 0.0f; };
+            auto ld_sb = [&](int kb) { return (BMODE == 0 && kb < num_kb) ? __ldg(sb_ptr + kb) : 0.0f; };
+            float sa0 = ld_sa(0), sb0 = ld_sb(0), sa1 = ld_sa(1), sb1 = ld_sb(1);
+            int kb = 0;
+            for (; kb + 1 < num_kb; kb += 2) {
+                if (!promote(sa0, sb0)) {
+                    ok = false;
+                    break;
+                }
+                sa0 = ld_sa(kb + 2);
+                sb0 = ld_sb(kb + 2);
+                if (!promote(sa1, sb1)) {
+                    ok = false;
+                    break;
+                }
+                sa1 = ld_sa(kb + 3);
+                sb1 = ld_sb(kb + 3);
             }
+            if (ok && kb < num_kb && !promote(sa0, sb0))
+                ok = false;
             if (!ok)
                 break;
 
