@@ -14,5 +14,6 @@ from .binding import (  # noqa: F401
     lib,
     quant_1x128,
     quant_128x128,
+    selftest_division,
     selftest_timeout,
 )

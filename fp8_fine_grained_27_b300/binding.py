@@ -21,7 +21,7 @@ OK, EINVAL, EALIGN, EARCH, ECUDA, ETIMEOUT = 0, -1, -2, -3, -4, -5
 EXPORTS = (
     "fp8_quant_1x128", "fp8_quant_128x128", "fp8_gemm_blockscaled", "fp8_grouped_gemm_moe",
     "fp8bs_e4m3_encode", "fp8bs_status_string", "fp8bs_get_device_error",
-    "fp8bs_selftest_timeout", "fp8bs_version",
+    "fp8bs_selftest_timeout", "fp8bs_selftest_division", "fp8bs_version",
 )
 
 
@@ -51,10 +51,11 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_status_string.restype = ctypes.c_char_p
         L.fp8bs_get_device_error.argtypes = [vp]
         L.fp8bs_selftest_timeout.argtypes = [i64, vp]
+        L.fp8bs_selftest_division.argtypes = [vp, vp]
         L.fp8bs_version.restype = ctypes.c_char_p
         for name in ("fp8_quant_1x128", "fp8_quant_128x128", "fp8_gemm_blockscaled",
                      "fp8_grouped_gemm_moe", "fp8bs_e4m3_encode", "fp8bs_get_device_error",
-                     "fp8bs_selftest_timeout"):
+                     "fp8bs_selftest_timeout", "fp8bs_selftest_division"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -140,6 +141,15 @@ def e4m3_encode(x: torch.Tensor, q=None, stream=None):
 
 def get_device_error(stream=None) -> int:
     return lib().fp8bs_get_device_error(_stream(stream))
+
+
+def selftest_division(stream=None):
+    """(code mismatches, quotient mismatches) of the fast quotient against the
+    IEEE divide over every BF16 (amax, x) pair with |x| <= amax."""
+    out = torch.zeros(2, dtype=torch.int64, device="cuda")
+    _check("fp8bs_selftest_division", lib().fp8bs_selftest_division(_ptr(out), _stream(stream)))
+    code, quot = out.tolist()
+    return code, quot
 
 
 def selftest_timeout(timeout_ns: int, stream=None):

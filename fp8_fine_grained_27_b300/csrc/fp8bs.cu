@@ -374,6 +374,21 @@ int fp8bs_e4m3_encode(const float *x, uint8_t *q, int64_t n, void *stream)
     return launch_status();
 }
 
+int fp8bs_selftest_division(unsigned long long *counts, void *stream)
+{
+    if (!counts)
+        return FP8BS_EINVAL;
+    DeviceInfo *d;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(counts, 0, 2 * sizeof(unsigned long long), st) != cudaSuccess)
+        return FP8BS_ECUDA;
+    quant::selftest_division_kernel<<<0x7F7F, 256, 0, st>>>(counts);
+    return launch_status();
+}
+
 int fp8bs_get_device_error(void *stream)
 {
     cudaStream_t st = static_cast<cudaStream_t>(stream);

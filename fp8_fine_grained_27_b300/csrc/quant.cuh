@@ -5,7 +5,8 @@
 // sign-cleared BF16 bit patterns (for finite inputs their unsigned order is
 // the order of magnitudes, so the maximum is exact), forms the scale
 // amax / 448 with an IEEE single-precision divide (1.0 for an all-zero tile)
-// and each code as E4M3_RNE_sat(x / scale), again with an IEEE divide.
+// and each code as E4M3_RNE_sat(x / scale), with the codes identical to those
+// of the IEEE single-precision quotient (see Quotient below).
 // All grids are persistent: a CTA walks tiles with a stride of gridDim.x.
 #pragma once
 #include <cstdint>
@@ -40,14 +41,43 @@ __device__ __forceinline__ float tile_scale(float amax)
     return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
 }
 
+// x / s for every x of a tile, by Markstein's division (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990): with r = RN(1/s) taken once per
+// tile, q0 = RN(x r), the remainder e = x - s q0 (one fused multiply-add) and
+// q = RN(q0 + e r) -- three floating-point operations per element instead of
+// a full IEEE divide.  q can differ from the IEEE quotient in its last bit
+// (near underflow), but its E4M3 code never does: fp8bs_selftest_division
+// encodes both for every BF16 amax and every BF16 x with |x| <= amax (about
+// 2^31 pairs) and finds no difference.  Tiles whose scale is below 2^-100
+// (reciprocal near overflow) keep the IEEE divide.
+struct Quotient {
+    float s, r;
+    bool fast;
+    __device__ __forceinline__ explicit Quotient(float scale)
+    {
+        s = scale;
+        r = __frcp_rn(scale);
+        fast = scale >= 0x1p-100f;
+    }
+    __device__ __forceinline__ float operator()(float x) const
+    {
+        if (!fast)
+            return __fdiv_rn(x, s);
+        const float q0 = __fmul_rn(x, r);
+        const float e = __fmaf_rn(-q0, s, x);
+        // s > 0, so the quotient carries x's sign; the correction step would
+        // turn -0 into +0, so the sign is restored explicitly
+        return copysignf(__fmaf_rn(e, r, q0), x);
+    }
+};
+
 // 8 BF16 values -> 8 codes (two 32-bit words, element j in byte j).
-__device__ __forceinline__ uint2 encode8(const uint4 &v, float s)
+__device__ __forceinline__ uint2 encode8(const uint4 &v, const Quotient &q)
 {
     uint2 r;
-    r.x = e4m3x2(__fdiv_rn(bf16lo(v.x), s), __fdiv_rn(bf16hi(v.x), s)) |
-          (e4m3x2(__fdiv_rn(bf16lo(v.y), s), __fdiv_rn(bf16hi(v.y), s)) << 16);
-    r.y = e4m3x2(__fdiv_rn(bf16lo(v.z), s), __fdiv_rn(bf16hi(v.z), s)) |
-          (e4m3x2(__fdiv_rn(bf16lo(v.w), s), __fdiv_rn(bf16hi(v.w), s)) << 16);
+    r.x = e4m3x2(q(bf16lo(v.x)), q(bf16hi(v.x))) | (e4m3x2(q(bf16lo(v.y)), q(bf16hi(v.y))) << 16);
+    r.y = e4m3x2(q(bf16lo(v.z)), q(bf16hi(v.z))) | (e4m3x2(q(bf16lo(v.w)), q(bf16hi(v.w))) << 16);
     return r;
 }
 
@@ -109,7 +139,7 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t *__
                 const float sc = tile_scale(pair_max_to_f32(a));
                 const int64_t m = m0 + r0 + 16 * p;
                 if (m < M) {
-                    *reinterpret_cast<uint2 *>(q + m * ldq + col) = encode8(v[p], sc);
+                    *reinterpret_cast<uint2 *>(q + m * ldq + col) = encode8(v[p], Quotient(sc));
                     if (c16 == 0)
                         s[kb * lds + m] = sc;
                 }
@@ -130,11 +160,12 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t *__
             for (int w = 1; w < kThreads / 32; ++w)
                 b = __vmaxu2(b, red[w]);
             const float sc = tile_scale(pair_max_to_f32(b));
+            const Quotient qt(sc);
 #pragma unroll
             for (int p = 0; p < 8; ++p) {
                 const int64_t m = m0 + r0 + 16 * p;
                 if (m < M)
-                    *reinterpret_cast<uint2 *>(q + m * ldq + col) = encode8(v[p], sc);
+                    *reinterpret_cast<uint2 *>(q + m * ldq + col) = encode8(v[p], qt);
             }
             if (tid == 0)
                 s[(m0 / 128) * lds + kb] = sc;
@@ -232,12 +263,12 @@ __global__ void __launch_bounds__(kThreads) quant_cols_kernel(const uint16_t *__
 #pragma unroll 1
         for (int i = 0; i < 8; ++i) {
             const int w = warp * 8 + i;
-            const float slo = sm.sc[2 * w], shi = sm.sc[2 * w + 1];
+            const Quotient qlo(sm.sc[2 * w]), qhi(sm.sc[2 * w + 1]);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int r = lane + 32 * j;
                 const uint32_t word = sm.xs[r * kColsPitch + w];
-                const uint32_t c2 = e4m3x2(__fdiv_rn(bf16lo(word), slo), __fdiv_rn(bf16hi(word), shi));
+                const uint32_t c2 = e4m3x2(qlo(bf16lo(word)), qhi(bf16hi(word)));
                 sm.qs[(2 * w) * 128 + r] = static_cast<uint8_t>(c2 & 0xFF);
                 sm.qs[(2 * w + 1) * 128 + r] = static_cast<uint8_t>(c2 >> 8);
             }
@@ -255,6 +286,38 @@ __global__ void __launch_bounds__(kThreads) quant_cols_kernel(const uint16_t *__
             }
         }
         __syncthreads();
+    }
+}
+
+// Exhaustive check of Quotient against the IEEE divide over the whole BF16
+// domain of the quantisers: block = one positive finite BF16 amax
+// (0x0001 .. 0x7F7F), threads = every BF16 x with |x| <= amax, both signs.
+// counts[0] += pairs whose E4M3 codes differ, counts[1] += pairs whose
+// single-precision quotients differ (diagnostic).
+__global__ void selftest_division_kernel(unsigned long long *counts)
+{
+    const uint32_t abits = blockIdx.x + 1;  // 0x0001 .. 0x7F7F
+    const float amax = __uint_as_float(abits << 16);
+    const float s = tile_scale(amax);
+    const Quotient q(s);
+    unsigned long long bad_code = 0, bad_quot = 0;
+    for (uint32_t xb = threadIdx.x; xb <= abits; xb += blockDim.x) {
+        for (uint32_t sign = 0; sign < 2; ++sign) {
+            const float x = __uint_as_float((xb | (sign << 15)) << 16);
+            const float fast = q(x), ieee = __fdiv_rn(x, s);
+            bad_quot += (__float_as_uint(fast) != __float_as_uint(ieee)) ? 1 : 0;
+            bad_code += ((e4m3x2(fast, 0.0f) & 0xFF) != (e4m3x2(ieee, 0.0f) & 0xFF)) ? 1 : 0;
+        }
+    }
+    for (int o = 16; o >= 1; o >>= 1) {
+        bad_code += __shfl_xor_sync(0xFFFFFFFFu, bad_code, o);
+        bad_quot += __shfl_xor_sync(0xFFFFFFFFu, bad_quot, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        if (bad_code)
+            atomicAdd(&counts[0], bad_code);
+        if (bad_quot)
+            atomicAdd(&counts[1], bad_quot);
     }
 }
 

@@ -15,8 +15,8 @@
  *     the forward and the backward pass.
  * Readings where the pages are silent: OCP E4M3FN (max 448); scale =
  * amax / 448 as an IEEE FP32 divide (1.0 for an all-zero tile); code =
- * E4M3(x / scale) with an IEEE FP32 divide, round-to-nearest-even, saturating
- * at +-448, sign kept.
+ * E4M3(x / scale) of the IEEE FP32 quotient, round-to-nearest-even,
+ * saturating at +-448, sign kept.
  *
  * Conventions for every call:
  *   - All pointers are DEVICE pointers owned by the caller, except where a
@@ -134,6 +134,17 @@ int fp8_grouped_gemm_moe(const uint8_t *A, int64_t lda, const float *sa, int64_t
  * A diagnostic for checking the conversion exhaustively.
  */
 int fp8bs_e4m3_encode(const float *x, uint8_t *q, int64_t n, void *stream);
+
+/*
+ * fp8bs_selftest_division -- the quantisers divide by the tile scale with a
+ * per-tile reciprocal and one Markstein correction instead of an IEEE divide.
+ * This diagnostic encodes both quotients to E4M3 for every positive finite
+ * BF16 amax and every BF16 x with |x| <= amax (about 2^31 pairs) and writes
+ * counts[0] = pairs whose codes differ (0 means the fast path is bit-exact on
+ * every BF16 input), counts[1] = pairs whose FP32 quotients differ.
+ * counts: DEVICE unsigned long long [2].
+ */
+int fp8bs_selftest_division(unsigned long long *counts, void *stream);
 
 /* Human-readable text for a status code (static storage). */
 const char *fp8bs_status_string(int status);

@@ -47,6 +47,17 @@ def _cols(fb, orc, x_bits):
     assert bad == 0, f"{bad} codes differ"
 
 
+def test_fast_quotient_equals_ieee_divide_on_whole_bf16_domain(fb):
+    """The quantisers divide by the tile scale with a per-tile reciprocal and
+    one Markstein correction; on the device, encode that quotient and the IEEE
+    quotient to E4M3 for every BF16 amax and every BF16 x with |x| <= amax:
+    the codes must agree everywhere (the FP32 quotients may differ in the
+    last bit near underflow, where both encode to zero)."""
+    code_mismatches, quotient_mismatches = fb.selftest_division()
+    assert code_mismatches == 0
+    assert quotient_mismatches < 2 ** 31 // 100
+
+
 def test_encode_exhaustive(fb, orc):
     """Every non-NaN FP32 bit pattern through the kernels' E4M3 conversion."""
     chunk = 1 << 28
@@ -135,3 +146,4 @@ def test_strided_views(fb, orc):
     torch.cuda.synchronize()
     qr, sr = orc.quant_1x128_rows(np.ascontiguousarray(a[:, :384]))
     assert np.array_equal(q.cpu().numpy(), qr) and np.array_equal(s.cpu().numpy(), sr)
+
