@@ -3,7 +3,10 @@
 
 One step = one pass of the whole hot path over one batch of the workload:
   mla   (default) A 4096x7168 BF16 -> 1x128 quantise; W_q 1536x7168 and
-        W_kv 576x7168 -> 128x128 quantise; two block-scaled GEMMs (BF16 out).
+        W_kv 576x7168 stored stacked as one 2112x7168 weight (1536 is a
+        multiple of 128, so no 128x128 block straddles the two) -> one
+        128x128 quantise and one GEMM whose column slices [0,1536) and
+        [1536,2112) are the q and kv latents (BF16 out).
   ffn   A 16384x7168 (Student-t), B 18432x7168: quantise both, one GEMM.
   wgrad dY 16384x2048, X 16384x7168: token-wise 1x128 quantise (transposed
         codes), dW = dY^T X with FP32 output.
@@ -107,7 +110,8 @@ class ClockSampler:
 def workload_desc(name):
     return {
         "mla": {"workload": "mla_down_proj", "M": 4096, "K": 7168, "N": [1536, 576],
-                "gemms": 2, "quant": "A 1x128, W_q/W_kv 128x128", "out": "bf16"},
+                "gemms": "2 (q 1536 + kv 576, one launch over the stacked 2112-row weight)",
+                "quant": "A 1x128, [W_q; W_kv] 128x128", "out": "bf16"},
         "ffn": {"workload": "dense_ffn", "M": 16384, "K": 7168, "N": [18432],
                 "gemms": 1, "quant": "A 1x128, B 128x128", "out": "bf16"},
         "wgrad": {"workload": "wgrad", "M": 2048, "K": 16384, "N": [7168],
@@ -151,7 +155,7 @@ class Step:
         self.kernels = []  # (label, kind) per launch, in order
         if name in ("mla", "tiny"):
             d = synth.mla(seed=seed) if name == "mla" else synth.tiny(seed=seed)
-            self.host = {"A": d["A"], "W": [d["Wq"], d["Wkv"]] if name == "mla" else [d["B"]]}
+            self.host = {"A": d["A"], "W": [np.concatenate([d["Wq"], d["Wkv"]])] if name == "mla" else [d["B"]]}
         elif name == "ffn":
             d = synth.ffn(seed=seed)
             self.host = {"A": d["A"], "W": [d["B"]]}

@@ -41,45 +41,70 @@ __device__ __forceinline__ float tile_scale(float amax)
     return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
 }
 
-// x / s for every x of a tile, by Markstein's division (P. Markstein,
-// "Computation of elementary functions on the IBM RISC System/6000
-// processor", IBM J. Res. Dev. 34(1), 1990): with r = RN(1/s) taken once per
-// tile, q0 = RN(x r), the remainder e = x - s q0 (one fused multiply-add) and
-// q = RN(q0 + e r) -- three floating-point operations per element instead of
-// a full IEEE divide.  q can differ from the IEEE quotient in its last bit
-// (near underflow), but its E4M3 code never does: fp8bs_selftest_division
-// encodes both for every BF16 amax and every BF16 x with |x| <= amax (about
-// 2^31 pairs) and finds no difference.  Tiles whose scale is below 2^-100
-// (reciprocal near overflow) keep the IEEE divide.
-struct Quotient {
-    float s, r;
-    bool fast;
-    __device__ __forceinline__ explicit Quotient(float scale)
-    {
-        s = scale;
-        r = __frcp_rn(scale);
-        fast = scale >= 0x1p-100f;
-    }
-    __device__ __forceinline__ float operator()(float x) const
-    {
-        if (!fast)
-            return __fdiv_rn(x, s);
-        const float q0 = __fmul_rn(x, r);
-        const float e = __fmaf_rn(-q0, s, x);
-        // s > 0, so the quotient carries x's sign; the correction step would
-        // turn -0 into +0, so the sign is restored explicitly
-        return copysignf(__fmaf_rn(e, r, q0), x);
-    }
-};
-
-// 8 BF16 values -> 8 codes (two 32-bit words, element j in byte j).
-__device__ __forceinline__ uint2 encode8(const uint4 &v, const Quotient &q)
+// x / s for the two values of a BF16 pair, by Markstein's division
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with r = RN(1/s)
+// taken once per tile, q0 = RN(x r), the remainder e = x - s q0 (one fused
+// multiply-add) and q = RN(q0 + e r) -- three floating-point operations per
+// value, issued two values at a time (f32x2), instead of a full IEEE divide.
+// q can differ from the IEEE quotient in its last bit (near underflow), but
+// its E4M3 code never does: fp8bs_selftest_division encodes both for every
+// BF16 amax and every BF16 x with |x| <= amax (about 2^31 pairs) and finds no
+// difference.  The low and high value may have different scales (two
+// columns of the transposed quantiser).  Scales below 2^-100 (reciprocal
+// near overflow) take the IEEE divide.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi)
 {
-    uint2 r;
-    r.x = e4m3x2(q(bf16lo(v.x)), q(bf16hi(v.x))) | (e4m3x2(q(bf16lo(v.y)), q(bf16hi(v.y))) << 16);
-    r.y = e4m3x2(q(bf16lo(v.z)), q(bf16hi(v.z))) | (e4m3x2(q(bf16lo(v.w)), q(bf16hi(v.w))) << 16);
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
     return r;
 }
+
+__device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+struct QuotientPair {
+    uint64_t r2, ns2;
+    float s_lo, s_hi;
+    bool fast;
+    __device__ __forceinline__ QuotientPair(float scale_lo, float scale_hi)
+    {
+        s_lo = scale_lo;
+        s_hi = scale_hi;
+        fast = scale_lo >= 0x1p-100f && scale_hi >= 0x1p-100f;
+        r2 = pack2(__frcp_rn(scale_lo), __frcp_rn(scale_hi));
+        ns2 = pack2(-scale_lo, -scale_hi);
+    }
+    // quotients of the two values of BF16 pair word w (low half first)
+    __device__ __forceinline__ void quot(uint32_t w, float &q_lo, float &q_hi) const
+    {
+        const float x_lo = bf16lo(w), x_hi = bf16hi(w);
+        if (fast) {
+            const uint64_t x2 = pack2(x_lo, x_hi);
+            uint64_t q0, e, q;
+            asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(x2), "l"(r2));
+            asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(q0), "l"(ns2), "l"(x2));
+            asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(e), "l"(r2), "l"(q0));
+            unpack2(q, q_lo, q_hi);
+            // s > 0, so a quotient carries x's sign; the correction step
+            // would turn -0 into +0, so the sign is restored explicitly
+            q_lo = copysignf(q_lo, x_lo);
+            q_hi = copysignf(q_hi, x_hi);
+        } else {
+            q_lo = __fdiv_rn(x_lo, s_lo);
+            q_hi = __fdiv_rn(x_hi, s_hi);
+        }
+    }
+    // E4M3 codes of the pair: low value in the low byte
+    __device__ __forceinline__ uint32_t codes(uint32_t w) const
+    {
+        float lo, hi;
+        quot(w, lo, hi);
+        return e4m3x2(lo, hi);
+    }
+};
 
 __device__ __forceinline__ uint4 ldg_stream(const void *p)
 {
@@ -91,11 +116,15 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p)
 }
 
 // ---------------------------------------------------------------------------
-// Tiles of 128 rows x 128 contiguous columns (one K chunk).  Thread t owns the
-// 16-byte column group t % 16 of rows t/16 + 16p (p = 0..7): eight loads in
-// flight per thread.
+// Tiles of 128 rows x 128 contiguous columns (one K chunk).  Four lanes share
+// a row (8 rows per warp instruction, so the per-row amax, scale and
+// reciprocal cost a quarter of what 16 lanes per row would); lane j of a
+// row owns the 16-byte column groups j, j+4, j+8, j+12, so each load
+// instruction reads 64 contiguous bytes per row and each code store writes
+// one full 32-byte sector per row.  A thread holds two rows (64 apart):
+// eight 16-byte loads in flight.
 //   kBlock = false: one scale per row per chunk (1x128 tiles), reduced over
-//                   the 16 lanes that share a row; s[kb*lds + m].
+//                   the row's 4 lanes; s[kb*lds + m].
 //   kBlock = true : one scale per 128x128 block, reduced over the CTA;
 //                   s[mb*lds + kb].
 // Tile order: kb fastest, so neighbouring CTAs read neighbouring columns.
@@ -108,69 +137,69 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t *__
 {
     __shared__ uint32_t red[kThreads / 32];
     const int tid = threadIdx.x;
-    const int c16 = tid & 15;
-    const int r0 = tid >> 4;
+    const int lane = tid & 31;
+    const int j = lane & 3;                       // column-group phase within the row
+    const int rw = (tid >> 5) * 8 + (lane >> 2);  // 0..63
     const int64_t nkb = K / 128;
     const int64_t ntiles = ((M + 127) / 128) * nkb;
 
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const int64_t kb = tile % nkb;
         const int64_t m0 = (tile / nkb) * 128;
-        const int64_t col = kb * 128 + c16 * 8;
-
-        uint4 v[8];
+        uint4 v[2][4];
 #pragma unroll
-        for (int p = 0; p < 8; ++p) {
-            const int64_t m = m0 + r0 + 16 * p;
-            if (m < M)
-                v[p] = ldg_stream(x + m * ldx + col);
-            else
-                v[p] = make_uint4(0, 0, 0, 0);
+        for (int rr = 0; rr < 2; ++rr) {
+            const int64_t m = m0 + rw + 64 * rr;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                v[rr][i] = (m < M) ? ldg_stream(x + m * ldx + kb * 128 + (j + 4 * i) * 8) : make_uint4(0, 0, 0, 0);
         }
-
+        uint32_t am[2];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr)
+            am[rr] = __vmaxu2(__vmaxu2(amax8(v[rr][0]), amax8(v[rr][1])), __vmaxu2(amax8(v[rr][2]), amax8(v[rr][3])));
+        float sc[2];
         if constexpr (!kBlock) {
 #pragma unroll
-            for (int p = 0; p < 8; ++p) {
-                uint32_t a = amax8(v[p]);
-                a = __vmaxu2(a, __shfl_xor_sync(0xFFFFFFFFu, a, 8));
-                a = __vmaxu2(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
+            for (int rr = 0; rr < 2; ++rr) {
+                uint32_t a = am[rr];
                 a = __vmaxu2(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
                 a = __vmaxu2(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-                const float sc = tile_scale(pair_max_to_f32(a));
-                const int64_t m = m0 + r0 + 16 * p;
-                if (m < M) {
-                    *reinterpret_cast<uint2 *>(q + m * ldq + col) = encode8(v[p], Quotient(sc));
-                    if (c16 == 0)
-                        s[kb * lds + m] = sc;
-                }
+                sc[rr] = tile_scale(pair_max_to_f32(a));
             }
         } else {
-            uint32_t a = amax8(v[0]);
-#pragma unroll
-            for (int p = 1; p < 8; ++p)
-                a = __vmaxu2(a, amax8(v[p]));
+            uint32_t a = __vmaxu2(am[0], am[1]);
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1)
                 a = __vmaxu2(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-            if ((tid & 31) == 0)
+            if (lane == 0)
                 red[tid >> 5] = a;
             __syncthreads();
             uint32_t b = red[0];
 #pragma unroll
             for (int w = 1; w < kThreads / 32; ++w)
                 b = __vmaxu2(b, red[w]);
-            const float sc = tile_scale(pair_max_to_f32(b));
-            const Quotient qt(sc);
-#pragma unroll
-            for (int p = 0; p < 8; ++p) {
-                const int64_t m = m0 + r0 + 16 * p;
-                if (m < M)
-                    *reinterpret_cast<uint2 *>(q + m * ldq + col) = encode8(v[p], qt);
-            }
-            if (tid == 0)
-                s[(m0 / 128) * lds + kb] = sc;
+            sc[0] = sc[1] = tile_scale(pair_max_to_f32(b));
             __syncthreads();  // red[] is rewritten by the next tile
         }
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int64_t m = m0 + rw + 64 * rr;
+            if (m < M) {
+                const QuotientPair qt(sc[rr], sc[rr]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    uint2 c;
+                    c.x = qt.codes(v[rr][i].x) | (qt.codes(v[rr][i].y) << 16);
+                    c.y = qt.codes(v[rr][i].z) | (qt.codes(v[rr][i].w) << 16);
+                    *reinterpret_cast<uint2 *>(q + m * ldq + kb * 128 + (j + 4 * i) * 8) = c;
+                }
+                if (!kBlock && j == 0)
+                    s[kb * lds + m] = sc[rr];
+            }
+        }
+        if (kBlock && tid == 0)
+            s[(m0 / 128) * lds + kb] = sc[0];
     }
 }
 
@@ -263,12 +292,12 @@ __global__ void __launch_bounds__(kThreads) quant_cols_kernel(const uint16_t *__
 #pragma unroll 1
         for (int i = 0; i < 8; ++i) {
             const int w = warp * 8 + i;
-            const Quotient qlo(sm.sc[2 * w]), qhi(sm.sc[2 * w + 1]);
+            const QuotientPair qp(sm.sc[2 * w], sm.sc[2 * w + 1]);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int r = lane + 32 * j;
                 const uint32_t word = sm.xs[r * kColsPitch + w];
-                const uint32_t c2 = e4m3x2(qlo(bf16lo(word)), qhi(bf16hi(word)));
+                const uint32_t c2 = qp.codes(word);
                 sm.qs[(2 * w) * 128 + r] = static_cast<uint8_t>(c2 & 0xFF);
                 sm.qs[(2 * w + 1) * 128 + r] = static_cast<uint8_t>(c2 >> 8);
             }
@@ -289,25 +318,27 @@ __global__ void __launch_bounds__(kThreads) quant_cols_kernel(const uint16_t *__
     }
 }
 
-// Exhaustive check of Quotient against the IEEE divide over the whole BF16
-// domain of the quantisers: block = one positive finite BF16 amax
-// (0x0001 .. 0x7F7F), threads = every BF16 x with |x| <= amax, both signs.
-// counts[0] += pairs whose E4M3 codes differ, counts[1] += pairs whose
-// single-precision quotients differ (diagnostic).
+// Exhaustive check of QuotientPair against the IEEE divide over the whole
+// BF16 domain of the quantisers: block = one positive finite BF16 amax
+// (0x0001 .. 0x7F7F), threads = every BF16 x with |x| <= amax, both signs
+// (x and -x form one pair word).  counts[0] += values whose E4M3 codes
+// differ, counts[1] += values whose single-precision quotients differ.
 __global__ void selftest_division_kernel(unsigned long long *counts)
 {
     const uint32_t abits = blockIdx.x + 1;  // 0x0001 .. 0x7F7F
     const float amax = __uint_as_float(abits << 16);
     const float s = tile_scale(amax);
-    const Quotient q(s);
+    const QuotientPair qp(s, s);
     unsigned long long bad_code = 0, bad_quot = 0;
     for (uint32_t xb = threadIdx.x; xb <= abits; xb += blockDim.x) {
-        for (uint32_t sign = 0; sign < 2; ++sign) {
-            const float x = __uint_as_float((xb | (sign << 15)) << 16);
-            const float fast = q(x), ieee = __fdiv_rn(x, s);
-            bad_quot += (__float_as_uint(fast) != __float_as_uint(ieee)) ? 1 : 0;
-            bad_code += ((e4m3x2(fast, 0.0f) & 0xFF) != (e4m3x2(ieee, 0.0f) & 0xFF)) ? 1 : 0;
-        }
+        const uint32_t w = xb | ((xb | 0x8000u) << 16);  // low: +x, high: -x
+        float q_lo, q_hi;
+        qp.quot(w, q_lo, q_hi);
+        const uint32_t codes = qp.codes(w);
+        const float i_lo = __fdiv_rn(bf16lo(w), s), i_hi = __fdiv_rn(bf16hi(w), s);
+        const uint32_t icodes = e4m3x2(i_lo, i_hi);
+        bad_quot += (__float_as_uint(q_lo) != __float_as_uint(i_lo)) + (__float_as_uint(q_hi) != __float_as_uint(i_hi));
+        bad_code += ((codes & 0xFF) != (icodes & 0xFF)) + ((codes >> 8) != (icodes >> 8));
     }
     for (int o = 16; o >= 1; o >>= 1) {
         bad_code += __shfl_xor_sync(0xFFFFFFFFu, bad_code, o);

@@ -194,3 +194,26 @@ def test_timeout_path_reports_and_recovers(fb):
     q, s = fb.quant_1x128(x)
     torch.cuda.synchronize()
     assert int(q[0, 0]) == 0x7E and float(s[0, 0]) == float(np.float32(1) / np.float32(448))
+
+
+def test_mla_stacked_weight_equals_separate(fb, orc):
+    """W_q (1536 rows) and W_kv (576 rows) stacked into one 2112-row weight:
+    the 128x128 blocks never straddle the two, so the stacked quantisation and
+    the single GEMM reproduce the separate ones bit for bit."""
+    d = synth.mla()
+    qa, sa = fb.quant_1x128(dev(d["A"]))
+    qq, sq = fb.quant_128x128(dev(d["Wq"]))
+    qk, sk = fb.quant_128x128(dev(d["Wkv"]))
+    qw, sw = fb.quant_128x128(dev(np.concatenate([d["Wq"], d["Wkv"]])))
+    assert torch.equal(qw[:1536], qq) and torch.equal(qw[1536:], qk)
+    assert torch.equal(sw[:12], sq) and torch.equal(sw[12:], sk)
+    C = fb.gemm_blockscaled(qa, sa, qw, sw, 0)
+    Cq = fb.gemm_blockscaled(qa, sa, qq, sq, 0)
+    Ck = fb.gemm_blockscaled(qa, sa, qk, sk, 0)
+    torch.cuda.synchronize()
+    assert torch.equal(C[:, :1536], Cq) and torch.equal(C[:, 1536:], Ck)
+    rows = sample_rows(4096, 64, seed=8, must=(0, 4095))
+    oqa, osa = orc.quant_1x128_rows(d["A"])
+    oqw, osw = orc.quant_128x128(np.concatenate([d["Wq"], d["Wkv"]]))
+    ref = orc.bf16_round(orc.gemm_blockscaled(oqa, osa, oqw, osw, 0, rows=rows))
+    assert_gemm_close(host_bits(C[torch.from_numpy(rows).cuda()]), ref, "mla stacked")
