@@ -16,4 +16,5 @@ from .binding import (  # noqa: F401
     quant_128x128,
     selftest_division,
     selftest_timeout,
+    set_gemm_tile_n,
 )

@@ -21,7 +21,7 @@ OK, EINVAL, EALIGN, EARCH, ECUDA, ETIMEOUT = 0, -1, -2, -3, -4, -5
 EXPORTS = (
     "fp8_quant_1x128", "fp8_quant_128x128", "fp8_gemm_blockscaled", "fp8_grouped_gemm_moe",
     "fp8bs_e4m3_encode", "fp8bs_status_string", "fp8bs_get_device_error",
-    "fp8bs_selftest_timeout", "fp8bs_selftest_division", "fp8bs_version",
+    "fp8bs_selftest_timeout", "fp8bs_selftest_division", "fp8bs_set_gemm_tile_n", "fp8bs_version",
 )
 
 
@@ -52,10 +52,11 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_get_device_error.argtypes = [vp]
         L.fp8bs_selftest_timeout.argtypes = [i64, vp]
         L.fp8bs_selftest_division.argtypes = [vp, vp]
+        L.fp8bs_set_gemm_tile_n.argtypes = [i32]
         L.fp8bs_version.restype = ctypes.c_char_p
         for name in ("fp8_quant_1x128", "fp8_quant_128x128", "fp8_gemm_blockscaled",
                      "fp8_grouped_gemm_moe", "fp8bs_e4m3_encode", "fp8bs_get_device_error",
-                     "fp8bs_selftest_timeout", "fp8bs_selftest_division"):
+                     "fp8bs_selftest_timeout", "fp8bs_selftest_division", "fp8bs_set_gemm_tile_n"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -137,6 +138,11 @@ def e4m3_encode(x: torch.Tensor, q=None, stream=None):
     q = torch.empty(x.shape, dtype=torch.uint8, device=x.device) if q is None else q
     _check("fp8bs_e4m3_encode", lib().fp8bs_e4m3_encode(_ptr(x), _ptr(q), x.numel(), _stream(stream)))
     return q
+
+
+def set_gemm_tile_n(bn: int) -> None:
+    """GEMM output tile width: 128, 192, 256, or 0 for automatic."""
+    _check("fp8bs_set_gemm_tile_n", lib().fp8bs_set_gemm_tile_n(bn))
 
 
 def get_device_error(stream=None) -> int:

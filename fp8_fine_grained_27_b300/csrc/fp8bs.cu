@@ -6,6 +6,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/fp8bs.h"
@@ -40,7 +41,7 @@ struct DeviceInfo {
     int quant_rows_ctas = 0;  // resident CTAs per SM, 1x128 and 128x128 kernels
     int quant_block_ctas = 0;
     int quant_cols_ctas = 0;
-    unsigned gemm_attr_set = 0;  // bit per GEMM instance: smem attribute applied
+    unsigned gemm_attr_set = 0;  // bit per GEMM instance: shared-memory attribute applied
 };
 
 std::mutex g_mu;
@@ -119,22 +120,56 @@ int make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t 
 }
 
 // ------------------------------------------------------------------ GEMM
-template <int BN, int STAGES, int BMODE, bool OUT_F32, bool GROUPED>
-int launch_gemm(DeviceInfo *d, int inst_bit, const CUtensorMap &tA, const CUtensorMap &tB, const CUtensorMap &tSB,
+template <int BN, int BMODE, bool OUT_F32, bool GROUPED>
+int launch_gemm(DeviceInfo *d, const CUtensorMap &tA, const CUtensorMap &tB, const CUtensorMap &tSB,
                 const gemm::Params &p, int grid, cudaStream_t st)
 {
-    using L = gemm::Layout<BN, STAGES, BMODE>;
-    auto kern = gemm::gemm_kernel<BN, STAGES, BMODE, OUT_F32, GROUPED>;
+    using C = gemm::Cfg<BN, BMODE, GROUPED>;
+    auto kern = gemm::gemm_kernel<BN, BMODE, OUT_F32, GROUPED>;
+    constexpr int inst_bit = (BN == 256 ? 0 : BN == 192 ? 1 : 2) * 8 + BMODE * 4 + (OUT_F32 ? 2 : 0) + (GROUPED ? 1 : 0);
     {
         std::lock_guard<std::mutex> lk(g_mu);
         if (!(d->gemm_attr_set & (1u << inst_bit))) {
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC) != cudaSuccess)
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::ALLOC) != cudaSuccess)
                 return FP8BS_ECUDA;
             d->gemm_attr_set |= (1u << inst_bit);
         }
     }
-    kern<<<grid, gemm::kThreads, L::ALLOC, st>>>(tA, tB, tSB, p);
+    kern<<<grid, C::THREADS, C::ALLOC, st>>>(tA, tB, tSB, p);
     return launch_status();
+}
+
+template <int BMODE, bool GROUPED>
+int launch_gemm_bn(int bn, int out_dtype, DeviceInfo *d, const CUtensorMap &tA, const CUtensorMap &tB,
+                   const CUtensorMap &tSB, const gemm::Params &p, int grid, cudaStream_t st)
+{
+    if constexpr (BMODE == 0) {
+        if (bn == 256)
+            return out_dtype == 0 ? launch_gemm<256, BMODE, false, GROUPED>(d, tA, tB, tSB, p, grid, st)
+                                  : launch_gemm<256, BMODE, true, GROUPED>(d, tA, tB, tSB, p, grid, st);
+        if (bn == 192)
+            return out_dtype == 0 ? launch_gemm<192, BMODE, false, GROUPED>(d, tA, tB, tSB, p, grid, st)
+                                  : launch_gemm<192, BMODE, true, GROUPED>(d, tA, tB, tSB, p, grid, st);
+    }
+    return out_dtype == 0 ? launch_gemm<128, BMODE, false, GROUPED>(d, tA, tB, tSB, p, grid, st)
+                          : launch_gemm<128, BMODE, true, GROUPED>(d, tA, tB, tSB, p, grid, st);
+}
+
+std::atomic<int> g_tile_n{0};  // fp8bs_set_gemm_tile_n: 0 = automatic
+
+// Output tile width.  Per-row B scales (b_scale_mode 1) use 128.
+int pick_bn(int64_t M, int64_t N, int b_scale_mode, int num_sms)
+{
+    (void)M;
+    (void)num_sms;
+    if (b_scale_mode != 0)
+        return 128;
+    const int forced = g_tile_n.load(std::memory_order_relaxed);
+    if (forced)
+        return forced;
+    if (N <= 128)
+        return 128;
+    return 256;
 }
 
 }  // namespace
@@ -281,8 +316,7 @@ int fp8_gemm_blockscaled(const uint8_t *A, int64_t lda, const float *sa, int64_t
     p.offs = nullptr;
     p.G = 0;
 
-    const bool wide = (b_scale_mode == 0) && N > 128;
-    const int BN = wide ? 256 : 128;
+    const int BN = pick_bn(M, N, b_scale_mode, d->num_sms);
     CUtensorMap tA, tB, tSB;
     std::memset(&tSB, 0, sizeof tSB);
     if (make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, lda, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -294,15 +328,9 @@ int fp8_gemm_blockscaled(const uint8_t *A, int64_t lda, const float *sa, int64_t
     const int64_t tiles = ((M + 127) / 128) * ((N + BN - 1) / BN);
     const int grid = static_cast<int>(std::min<int64_t>(tiles, d->num_sms));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (b_scale_mode == 0) {
-        if (wide)
-            return out_dtype == 0 ? launch_gemm<256, 4, 0, false, false>(d, 0, tA, tB, tSB, p, grid, st)
-                                  : launch_gemm<256, 4, 0, true, false>(d, 1, tA, tB, tSB, p, grid, st);
-        return out_dtype == 0 ? launch_gemm<128, 6, 0, false, false>(d, 2, tA, tB, tSB, p, grid, st)
-                              : launch_gemm<128, 6, 0, true, false>(d, 3, tA, tB, tSB, p, grid, st);
-    }
-    return out_dtype == 0 ? launch_gemm<128, 6, 1, false, false>(d, 4, tA, tB, tSB, p, grid, st)
-                          : launch_gemm<128, 6, 1, true, false>(d, 5, tA, tB, tSB, p, grid, st);
+    if (b_scale_mode == 0)
+        return launch_gemm_bn<0, false>(BN, out_dtype, d, tA, tB, tSB, p, grid, st);
+    return launch_gemm_bn<1, false>(BN, out_dtype, d, tA, tB, tSB, p, grid, st);
 }
 
 int fp8_grouped_gemm_moe(const uint8_t *A, int64_t lda, const float *sa, int64_t ldsa, const uint8_t *B,
@@ -339,8 +367,7 @@ int fp8_grouped_gemm_moe(const uint8_t *A, int64_t lda, const float *sa, int64_t
     p.offs = group_offsets;
     p.G = G;
 
-    const bool wide = N > 128;
-    const int BN = wide ? 256 : 128;
+    const int BN = pick_bn(M_total, N, 0, d->num_sms);
     CUtensorMap tA, tB, tSB;
     std::memset(&tSB, 0, sizeof tSB);
     if (make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M_total, lda, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -349,12 +376,7 @@ int fp8_grouped_gemm_moe(const uint8_t *A, int64_t lda, const float *sa, int64_t
     // upper bound on the tile count without reading the offsets on the host
     const int64_t max_tiles = ((M_total + 127) / 128 + G) * ((N + BN - 1) / BN);
     const int grid = static_cast<int>(std::min<int64_t>(max_tiles, d->num_sms));
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (wide)
-        return out_dtype == 0 ? launch_gemm<256, 4, 0, false, true>(d, 6, tA, tB, tSB, p, grid, st)
-                              : launch_gemm<256, 4, 0, true, true>(d, 7, tA, tB, tSB, p, grid, st);
-    return out_dtype == 0 ? launch_gemm<128, 6, 0, false, true>(d, 8, tA, tB, tSB, p, grid, st)
-                          : launch_gemm<128, 6, 0, true, true>(d, 9, tA, tB, tSB, p, grid, st);
+    return launch_gemm_bn<0, true>(BN, out_dtype, d, tA, tB, tSB, p, grid, static_cast<cudaStream_t>(stream));
 }
 
 int fp8bs_e4m3_encode(const float *x, uint8_t *q, int64_t n, void *stream)
@@ -387,6 +409,14 @@ int fp8bs_selftest_division(unsigned long long *counts, void *stream)
         return FP8BS_ECUDA;
     quant::selftest_division_kernel<<<0x7F7F, 256, 0, st>>>(counts);
     return launch_status();
+}
+
+int fp8bs_set_gemm_tile_n(int bn)
+{
+    if (bn != 0 && bn != 128 && bn != 192 && bn != 256)
+        return FP8BS_EINVAL;
+    g_tile_n.store(bn, std::memory_order_relaxed);
+    return FP8BS_OK;
 }
 
 int fp8bs_get_device_error(void *stream)

@@ -11,8 +11,7 @@
 //     acc[m][n] = fmaf(sa[kb][m] * sb(n, kb), P_kb[m][n], acc[m][n]),
 // while the MMA warp already fills the other TMEM buffer with chunk kb+1.
 //
-// CTA layout (384 threads = 3 warpgroups, one CTA per SM, persistent over
-// output tiles):
+// CTA layout (persistent, one CTA per SM), for an output tile 128 x BN:
 //   warp 0      TMA producer: A and B K-chunks (128 bytes of K per row, the
 //               128-byte swizzle) into a STAGES-deep shared-memory ring.
 //   warps 1, 3  MMA issuers (one thread each): warp 1 issues the even K
@@ -21,16 +20,21 @@
 //               execute, so two issuers keep the tensor pipe fed; each one
 //               commits its own chunks.  Warp 1 also owns the TMEM allocation.
 //   warp 2      idle.  Warpgroup 0 gives registers away (setmaxnreg 40).
-//   warps 4..11 promotion + epilogue (setmaxnreg 232: 128 FP32 accumulators
-//               per thread).  Warp w may only read TMEM lanes
-//               32*(w%4) .. 32*(w%4)+31; warps 4..7 cover the left half of the
-//               tile's columns, warps 8..11 the right half.
+//   warps 4..   promotion + epilogue, NWG warpgroups (setmaxnreg raised).
+//               Warp w reads TMEM lanes 32*(w%4) .. +31 (its 32 tile rows);
+//               warpgroup g owns columns [g*CPW, (g+1)*CPW) of the tile.
+//   BN = 256: 2 promotion warpgroups x 128 columns, 2 TMEM partials
+//             (four 32-column TMEM loads per chunk, software-pipelined);
+//   BN = 192: 3 promotion warpgroups x 64 columns, 2 TMEM partials;
+//   BN = 128: 2 promotion warpgroups x 64 columns, 4 TMEM partials.
+//   With 64 columns per thread both 32-column loads of a chunk are issued
+//   before a single wait.
 //
 // Synchronisation (all mbarriers, all waits bounded):
 //   full[s]   TMA bytes of stage s landed          (producer -> MMA)
 //   empty[s]  MMAs reading stage s are complete    (tcgen05.commit -> producer)
 //   tfull[b]  partial in TMEM buffer b is complete (tcgen05.commit -> promotion)
-//   tempty[b] promotion has read buffer b          (8 warp arrivals -> MMA)
+//   tempty[b] promotion has read buffer b          (one arrival per promotion warp -> MMA)
 //   sbfull/sbempty  per-stage B row scales (row-scale mode only)
 #pragma once
 #include <cstdint>
@@ -42,29 +46,55 @@ namespace gemm {
 
 constexpr int BM = 128;
 constexpr int BK = 128;
-constexpr int kThreads = 384;
 constexpr int kFirstPromoWarp = 4;
-constexpr int kPromoWarps = 8;
 constexpr int kGroupM = 16;      // raster: 16 M tiles share each sweep over N
 constexpr int kMaxGroups = 1024; // grouped GEMM: experts per call
+constexpr int kMaxSmem = 232448; // dynamic shared memory per CTA on sm_103
 
-template <int BN, int STAGES, int BMODE>
-struct Layout {
+template <int BN_, int BMODE_, bool GROUPED_>
+struct Cfg {
+    static constexpr int BN = BN_;
+    static constexpr int CPW = (BN == 256) ? 128 : 64;  // columns per promotion thread
+    static constexpr int NWG = BN / CPW;                // promotion warpgroups
+    static constexpr int NPW = 4 * NWG;                 // promotion warps
+    static constexpr int THREADS = 128 * (1 + NWG);
+    static constexpr int NP = CPW / 32;                 // 32-column TMEM loads per chunk
+    static constexpr int NTMEM = (BN <= 128) ? 4 : 2;   // TMEM partial buffers
+    static constexpr int TMEM_COLS = 512;
+    // registers: warpgroup 0 drops to 40; the promotion warpgroups share the
+    // rest of the launch's pool (THREADS x launch registers, 168 at 384
+    // threads, 128 at 512 threads)
+    static constexpr int LAUNCH_REGS = (THREADS == 384) ? 168 : 128;
+    static constexpr int PROMO_REGS = ((THREADS * LAUNCH_REGS - 128 * 40) / (128 * NWG)) / 8 * 8;
+    static_assert(128 * 40 + 128 * NWG * PROMO_REGS <= THREADS * LAUNCH_REGS, "setmaxnreg split exceeds the pool");
+    static_assert(PROMO_REGS <= 256 && PROMO_REGS >= CPW + 64 + 16, "promotion registers");
+    static_assert(NTMEM * BN <= TMEM_COLS, "TMEM partials");
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
-    static constexpr int SBROW_BYTES = (BMODE == 1) ? BN * 4 : 0;
-    static constexpr int EPI_BYTES = kPromoWarps * 2048;
+    static constexpr int SBROW_BYTES = (BMODE_ == 1) ? BN * 4 : 0;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SBROW_BYTES;
+    static constexpr int EPI_BYTES = NPW * 2048;
+    static constexpr int TABLE_BYTES = GROUPED_ ? (kMaxGroups + 1) * 4 : 0;
+    static constexpr int FIXED = EPI_BYTES + TABLE_BYTES + 512 + 1024;  // + barriers, + alignment slack
+    // Even, so that every use of a stage falls to the same MMA issuer (chunks
+    // c and c + STAGES have the same parity): each issuer then waits the
+    // phases of its stages in order and can never mistake a stage's previous
+    // completed phase for the one it needs.
+    static constexpr int FIT = (kMaxSmem - FIXED) / STAGE_BYTES;
+    static constexpr int STAGES = (FIT < 6 ? FIT : 6) / 2 * 2;
+    static_assert(STAGES >= 4 && STAGES % 2 == 0, "pipeline depth");
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SBROW = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_EPI = OFF_SBROW + STAGES * SBROW_BYTES;
     static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
-    static constexpr int NBAR = 4 * STAGES + 4;
+    static constexpr int NBAR = 4 * STAGES + 2 * NTMEM;
     static constexpr int OFF_TMEMSLOT = OFF_BAR + NBAR * 8;
     static constexpr int OFF_TILESTART = (OFF_TMEMSLOT + 4 + 15) / 16 * 16;
-    static constexpr int BYTES = OFF_TILESTART + (kMaxGroups + 1) * 4;
+    static constexpr int BYTES = OFF_TILESTART + TABLE_BYTES;
     static constexpr int ALLOC = BYTES + 1024;  // slack for 1024-byte alignment
-    static constexpr int TMEM_COLS = 2 * BN;    // double-buffered FP32 partials
+    static_assert(NBAR * 8 + 32 <= 512, "barrier area");
+    static_assert(ALLOC <= kMaxSmem, "shared memory per CTA");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
 };
 
@@ -135,13 +165,13 @@ __device__ __forceinline__ Tile tile_of(int t, const Params &p, const int *tile_
 
 // Prefix sum of per-expert tile counts, computed by the promotion warps.
 // Malformed ranges (negative length or past M) count as empty.
-template <int BN>
+template <int BN, int NPW>
 __device__ void build_tile_start(const Params &p, int *tile_start, int ptid)
 {
     const int num_n = (p.N + BN - 1) / BN;
-    __shared__ int warp_sums[kPromoWarps];
-    // each promotion thread owns up to 4 consecutive experts
-    constexpr int PER = (kMaxGroups + kPromoWarps * 32 - 1) / (kPromoWarps * 32);
+    __shared__ int warp_sums[NPW];
+    // each promotion thread owns up to PER consecutive experts
+    constexpr int PER = (kMaxGroups + NPW * 32 - 1) / (NPW * 32);
     int cnt[PER];
     int local = 0;
 #pragma unroll
@@ -167,7 +197,7 @@ __device__ void build_tile_start(const Params &p, int *tile_start, int ptid)
     }
     if (lane == 31)
         warp_sums[w] = incl;
-    asm volatile("bar.sync 1, %0;" ::"n"(kPromoWarps * 32));
+    asm volatile("bar.sync 1, %0;" ::"n"(NPW * 32));
     int before = 0;
     for (int i = 0; i < w; ++i)
         before += warp_sums[i];
@@ -179,7 +209,7 @@ __device__ void build_tile_start(const Params &p, int *tile_start, int ptid)
             tile_start[e] = run;
         run += cnt[i];
     }
-    if (ptid == kPromoWarps * 32 - 1)
+    if (ptid == NPW * 32 - 1)
         tile_start[p.G] = run;
 }
 
@@ -205,12 +235,33 @@ __device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[32])
                  : "memory");
 }
 
-template <int BN, int STAGES, int BMODE, bool OUT_F32, bool GROUPED>
-__global__ void __launch_bounds__(kThreads, 1)
+// Wait for both outstanding tcgen05.ld of this warp and tie their registers
+// to the wait, so that no use of them is scheduled before it.
+__device__ __forceinline__ void tmem_ld_wait_regs2(uint32_t (&r)[32], uint32_t (&q)[32])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+                   "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                   "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]), "+r"(q[0]), "+r"(q[1]), "+r"(q[2]),
+                   "+r"(q[3]), "+r"(q[4]), "+r"(q[5]), "+r"(q[6]), "+r"(q[7]), "+r"(q[8]), "+r"(q[9]),
+                   "+r"(q[10]), "+r"(q[11]), "+r"(q[12]), "+r"(q[13]), "+r"(q[14]), "+r"(q[15]), "+r"(q[16]),
+                   "+r"(q[17]), "+r"(q[18]), "+r"(q[19]), "+r"(q[20]), "+r"(q[21]), "+r"(q[22]), "+r"(q[23]),
+                   "+r"(q[24]), "+r"(q[25]), "+r"(q[26]), "+r"(q[27]), "+r"(q[28]), "+r"(q[29]), "+r"(q[30]),
+                   "+r"(q[31])
+                 :
+                 : "memory");
+}
+
+template <int BN, int BMODE, bool OUT_F32, bool GROUPED>
+__global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSB, const Params p)
 {
-    using L = Layout<BN, STAGES, BMODE>;
+    using L = Cfg<BN, BMODE, GROUPED>;
+    constexpr int STAGES = L::STAGES;
+    constexpr int NTMEM = L::NTMEM;
     extern __shared__ uint8_t dyn_smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(dyn_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -218,12 +269,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    uint32_t bar_full = sbase + L::OFF_BAR;
-    uint32_t bar_empty = bar_full + 8 * STAGES;
-    uint32_t bar_sbfull = bar_empty + 8 * STAGES;
-    uint32_t bar_sbempty = bar_sbfull + 8 * STAGES;
-    uint32_t bar_tfull = bar_sbempty + 8 * STAGES;
-    uint32_t bar_tempty = bar_tfull + 16;
+    const uint32_t bar_full = sbase + L::OFF_BAR;
+    const uint32_t bar_empty = bar_full + 8 * STAGES;
+    const uint32_t bar_sbfull = bar_empty + 8 * STAGES;
+    const uint32_t bar_sbempty = bar_sbfull + 8 * STAGES;
+    const uint32_t bar_tfull = bar_sbempty + 8 * STAGES;
+    const uint32_t bar_tempty = bar_tfull + 8 * NTMEM;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_TMEMSLOT);
     int *tile_start = reinterpret_cast<int *>(smem + L::OFF_TILESTART);
 
@@ -232,11 +283,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
             mbar_init(bar_sbfull + 8 * s, 1);
-            mbar_init(bar_sbempty + 8 * s, kPromoWarps);
+            mbar_init(bar_sbempty + 8 * s, L::NPW);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NTMEM; ++b) {
             mbar_init(bar_tfull + 8 * b, 1);
-            mbar_init(bar_tempty + 8 * b, kPromoWarps);
+            mbar_init(bar_tempty + 8 * b, L::NPW);
         }
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -253,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if constexpr (GROUPED) {
         if (warp >= kFirstPromoWarp)
-            build_tile_start<BN>(p, tile_start, threadIdx.x - kFirstPromoWarp * 32);
+            build_tile_start<BN, L::NPW>(p, tile_start, threadIdx.x - kFirstPromoWarp * 32);
     }
     tc_fence_before();
     __syncthreads();
@@ -314,8 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         continue;
                     const int s = c % STAGES;
                     const uint32_t ph = (c / STAGES) & 1;
-                    const int b = c & 1;
-                    const uint32_t tph = (c >> 1) & 1;
+                    const int b = c % NTMEM;
+                    const uint32_t tph = (c / NTMEM) & 1;
                     if (!mbar_wait(bar_tempty + 8 * b, tph ^ 1, ERR_TIMEOUT_MMA) ||
                         !mbar_wait(bar_full + 8 * s, ph, ERR_TIMEOUT_MMA)) {
                         ok = false;
@@ -339,20 +390,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     --d;
                 if (d > 0) {
                     --d;
-                    mbar_wait(bar_tfull + 8 * (d & 1), (d >> 1) & 1, ERR_TIMEOUT_MMA, 100000000ull);
+                    mbar_wait(bar_tfull + 8 * (d % NTMEM), (d / NTMEM) & 1, ERR_TIMEOUT_MMA, 100000000ull);
                 }
             }
         }
     } else {
-        regs_inc<232>();
+        regs_inc<L::PROMO_REGS>();
         // ------------------------------------------------------------ promotion + epilogue
+        constexpr int CPW = L::CPW;
+        constexpr int NP = L::NP;
         const int pw = warp - kFirstPromoWarp;
         const int quarter = warp & 3;
-        const int half = pw >> 2;
-        constexpr int HALF = BN / 2;  // columns per thread
-        constexpr int NP = HALF / 32; // 32-column pieces
+        const int grp = pw >> 2;
         const int row = quarter * 32 + lane;
-        const int col0 = half * HALF;
+        const int col0 = grp * CPW;
         const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
         uint8_t *epi = smem + L::OFF_EPI + pw * 2048;
         const float *sbrow_smem = reinterpret_cast<const float *>(smem + L::OFF_SBROW);
@@ -363,20 +414,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Tile tl = tile_of<BN, GROUPED>(t, p, tile_start);
             const int m_row = min(tl.m0 + row, p.M - 1);
             const float *sa_ptr = p.sa + m_row;
+            // CPW columns starting at a multiple of CPW never straddle a
+            // 128-column scale block
             int nb = (tl.n0 + col0) / 128;
             nb = min(nb, (p.N - 1) / 128);
             const float *sb_ptr = tl.sbp + static_cast<int64_t>(nb) * p.ldsb;
 
-            float acc[HALF];
+            float acc[CPW];
 #pragma unroll
-            for (int j = 0; j < HALF; ++j)
+            for (int j = 0; j < CPW; ++j)
                 acc[j] = 0.0f;
 
             // One K chunk: wait for its partial, read it from TMEM, release the
             // buffer, fold it into acc with the chunk's scales.
             auto promote = [&](float sa_v, float sb_v) -> bool {
-                const int b = c & 1;
-                const uint32_t tph = (c >> 1) & 1;
+                const int b = c % NTMEM;
+                const uint32_t tph = (c / NTMEM) & 1;
                 const int s = c % STAGES;
                 // every lane waits, then the warp reconverges before the
                 // .sync.aligned TMEM loads
@@ -391,21 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float *sbr = sbrow_smem + s * BN + col0;
                 (void)sbr;
 
-                uint32_t ra[32], rb[32];
-                tmem_ld32(taddr, ra);
-                tmem_ld_wait_regs(ra);
-                if constexpr (NP == 1) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(bar_tempty + 8 * b);
-                }
-#pragma unroll
-                for (int pc = 0; pc < NP; ++pc) {
-                    uint32_t(&cur)[32] = (pc & 1) ? rb : ra;
-                    uint32_t(&nxt)[32] = (pc & 1) ? ra : rb;
-                    if (pc + 1 < NP)
-                        tmem_ld32(taddr + (pc + 1) * 32, nxt);
+                auto fold = [&](int pc, const uint32_t(&cur)[32]) {
                     if constexpr (BMODE == 0) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
@@ -420,14 +459,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                             acc[pc * 32 + j + 3] = fmaf(sa_v * sb4.w, __uint_as_float(cur[j + 3]), acc[pc * 32 + j + 3]);
                         }
                     }
-                    if (pc + 1 < NP) {
-                        tmem_ld_wait_regs(nxt);
-                        if (pc + 2 == NP) {
-                            // the last piece is in registers: release the TMEM buffer
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0)
-                                mbar_arrive(bar_tempty + 8 * b);
+                };
+                auto release = [&]() {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(bar_tempty + 8 * b);
+                };
+
+                uint32_t ra[32], rb[32];
+                if constexpr (NP == 2) {
+                    // both loads in flight, one wait, release, then fold
+                    tmem_ld32(taddr, ra);
+                    tmem_ld32(taddr + 32, rb);
+                    tmem_ld_wait_regs2(ra, rb);
+                    release();
+                    fold(0, ra);
+                    fold(1, rb);
+                } else {
+                    // four loads, each overlapped with the fold of the previous one
+                    tmem_ld32(taddr, ra);
+                    tmem_ld_wait_regs(ra);
+#pragma unroll
+                    for (int pc = 0; pc < NP; ++pc) {
+                        uint32_t(&cur)[32] = (pc & 1) ? rb : ra;
+                        uint32_t(&nxt)[32] = (pc & 1) ? ra : rb;
+                        if (pc + 1 < NP)
+                            tmem_ld32(taddr + (pc + 1) * 32, nxt);
+                        fold(pc, cur);
+                        if (pc + 1 < NP) {
+                            tmem_ld_wait_regs(nxt);
+                            if (pc + 2 == NP)
+                                release();  // the last piece is in registers
                         }
                     }
                 }
@@ -475,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr int COLS_PER_ROUND = OUT_F32 ? 16 : 32;
             constexpr int ELEMS_PER_CHUNK = OUT_F32 ? 4 : 8;
 #pragma unroll
-            for (int g = 0; g < HALF / COLS_PER_ROUND; ++g) {
+            for (int g = 0; g < CPW / COLS_PER_ROUND; ++g) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const float *a = &acc[g * COLS_PER_ROUND + j * ELEMS_PER_CHUNK];

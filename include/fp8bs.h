@@ -146,6 +146,15 @@ int fp8bs_e4m3_encode(const float *x, uint8_t *q, int64_t n, void *stream);
  */
 int fp8bs_selftest_division(unsigned long long *counts, void *stream);
 
+/*
+ * fp8bs_set_gemm_tile_n -- output tile width (N per CTA tile) of both GEMM
+ * entry points for block-scaled B: 128, 192 or 256, or 0 to let the library
+ * choose from the problem shape (the default).  Process-wide; results do not
+ * depend on it (every output element is computed the same way), only speed.
+ * Per-row B scales (b_scale_mode 1) always use 128.
+ */
+int fp8bs_set_gemm_tile_n(int bn);
+
 /* Human-readable text for a status code (static storage). */
 const char *fp8bs_status_string(int status);
 

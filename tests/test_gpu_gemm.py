@@ -23,6 +23,13 @@ def fb():
     return fb
 
 
+@pytest.fixture(params=[0, 128, 192, 256], ids=["auto", "bn128", "bn192", "bn256"])
+def tile_n(request, fb):
+    fb.set_gemm_tile_n(request.param)
+    yield request.param
+    fb.set_gemm_tile_n(0)
+
+
 def _dense(fb, orc, a_bits, w_bits, out_dtype=torch.bfloat16, rows=None, what=""):
     qa, sa = fb.quant_1x128(dev(a_bits))
     qb, sb = fb.quant_128x128(dev(w_bits))
@@ -46,14 +53,14 @@ def test_tiny_workload(fb, orc):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 8, 128), (300, 392, 640), (129, 72, 256), (257, 520, 384), (64, 128, 1024)])
-def test_ragged_shapes(fb, orc, M, N, K):
+def test_ragged_shapes(fb, orc, tile_n, M, N, K):
     a = synth.fill_bf16(synth.OUTLIER, synth.key(80, M), (M, K), 1.0, 0.01, 50.0, k2=synth.key(81, M))
     w = synth.fill_bf16(synth.NORMAL, synth.key(82, N), (N, K), 0.02)
     _dense(fb, orc, a, w, what=f"{M}x{N}x{K}")
     _dense(fb, orc, a, w, out_dtype=torch.float32, what=f"{M}x{N}x{K} fp32")
 
 
-def test_mla_full(fb, orc):
+def test_mla_full(fb, orc, tile_n):
     """Both MLA down-projections, every output checked."""
     d = synth.mla()
     _dense(fb, orc, d["A"], d["Wq"], what="mla q")
@@ -123,7 +130,7 @@ def _grouped(fb, orc, a_bits, offs, w_bits, rows=None, what=""):
 
 
 @pytest.mark.parametrize("N", [256, 136, 64])
-def test_grouped_small_skewed(fb, orc, N):
+def test_grouped_small_skewed(fb, orc, tile_n, N):
     sizes = [0, 5, 0, 128, 129, 1, 300, 0, 64, 256, 0, 0, 77, 2, 0, 31]
     offs = np.concatenate([[0], np.cumsum(sizes)])
     M = int(offs[-1]) + 10  # trailing rows belong to no expert
@@ -133,7 +140,7 @@ def test_grouped_small_skewed(fb, orc, N):
     _grouped(fb, orc, a, offs, w, what=f"grouped N={N}")
 
 
-def test_grouped_256_experts_routed(fb, orc):
+def test_grouped_256_experts_routed(fb, orc, tile_n):
     """256 experts, top-8 routing of 512 tokens (skewed groups, many empty)."""
     tok = synth.moe_tokens(T=512, D=256)
     offs, token_of_row = synth.moe_route(tok, E=256, topk=8)
