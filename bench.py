@@ -40,6 +40,35 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
+PROFILES = os.path.join(ROOT, "profiles")
+GEMM_PROFILE = {"mla": "gemm_kernel_mla_4096x2112x7168.md"}
+
+
+def kernel_source_hash(files):
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "fp8_fine_grained_27_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per GEMM launch from the committed ncu summary of this
+    workload, or None if there is none or the kernel source changed since."""
+    name = GEMM_PROFILE.get(workload)
+    if not name:
+        return None
+    try:
+        text = open(os.path.join(PROFILES, name)).read()
+    except OSError:
+        return None
+    fields = dict(l.split(":", 1) for l in text.splitlines() if l.startswith(("kernel_source_sha256_16:", "traffic_bytes_per_launch:")))
+    if fields.get("kernel_source_sha256_16", "").split()[0:1] != [kernel_source_hash(["gemm.cuh", "ptx.cuh"])]:
+        return None
+    return int(fields["traffic_bytes_per_launch"].split()[0])
+
+
 def load_peaks():
     try:
         with open(PEAKS_FILE) as f:
@@ -233,6 +262,23 @@ class Step:
         return [("A", self.host["A"])]
 
 
+# ------------------------------------------------------------------ ranks
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The slowest rank's value (the job's step time under weak scaling)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, seconds_slowest: float, world: int) -> float:
+    """Whole-job throughput of `world` replicas that each process
+    units_per_rank in their own time; the job ends with the slowest rank."""
+    return world * units_per_rank / seconds_slowest
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args, rank, world):
     import torch
@@ -285,15 +331,11 @@ def run_ours(args, rank, world):
     for k in range(args.steps):
         for j, (label, _) in enumerate(launches):
             per_kernel.setdefault(label, []).append(ev[k][j].elapsed_time(ev[k][j + 1]))
-    ms_step = float(np.mean(per_step))
-    if dist:
-        t = torch.tensor([ms_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(float(np.mean(per_step)), dist, "cuda")
 
     flops = gemm_flops(args.workload)
     qbytes = quant_bytes(args.workload)
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = job_throughput(flops, ms_step * 1e-3, world) / 1e12
     peaks, peaks_src = load_peaks()
     fp8_peak = 2.0 * peaks["bf16_tflops"]
     # GEMM launches of one step (there may be several): their summed mean duration
@@ -319,7 +361,9 @@ def run_ours(args, rank, world):
         "config": {**workload_desc(args.workload), "l2": f"flushed ({args.flush_mb} MB write) before every step",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(fp8_peak, 1),
-                     "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
+                     "traffic": profiled_traffic(args.workload),
+                     "traffic_note": "DRAM read+write bytes per GEMM launch, ncu (profiles/), null if the kernel changed since",
                      "peak_source": f"{peaks_src}: 2 x bf16_tflops (dense FP8 = 2 x BF16)",
                      "kernel": "gemm_kernel", "kernel_ms": round(gemm_ms, 5)},
         "quant": {"achieved_gbs": round(quant_gbs, 1), "peak_gbs": peaks["hbm_gbs"],
@@ -373,12 +417,8 @@ def run_e2e(args, step, torch, fb, launches, flops, world, dist):
         for o, h in zip(outs, out_host):
             h.copy_(o, non_blocking=True)
     torch.cuda.synchronize()
-    dt = (time.perf_counter() - t0) / n
-    if dist:
-        t = torch.tensor([dt], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dt = float(t.item())
-    return {"value": round(world * flops / dt / 1e12, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+    dt = max_over_ranks((time.perf_counter() - t0) / n, dist, "cuda")
+    return {"value": round(job_throughput(flops, dt, world) / 1e12, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": n, "ms_per_step": round(dt * 1e3, 4)}
 
 
