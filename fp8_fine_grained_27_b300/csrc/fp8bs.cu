@@ -143,6 +143,9 @@ template <int BMODE, bool GROUPED>
 int launch_gemm_bn(int bn, int out_dtype, DeviceInfo *d, const CUtensorMap &tA, const CUtensorMap &tB,
                    const CUtensorMap &tSB, const gemm::Params &p, int grid, cudaStream_t st)
 {
+    if (bn == 256)
+        return out_dtype == 0 ? launch_gemm<256, BMODE, false, GROUPED>(d, tA, tB, tSB, p, grid, st)
+                              : launch_gemm<256, BMODE, true, GROUPED>(d, tA, tB, tSB, p, grid, st);
     if constexpr (BMODE == 0) {
         if (bn == 256)
             return out_dtype == 0 ? launch_gemm<256, BMODE, false, GROUPED>(d, tA, tB, tSB, p, grid, st)
@@ -162,9 +165,13 @@ int pick_bn(int64_t M, int64_t N, int b_scale_mode, int num_sms)
 {
     (void)M;
     (void)num_sms;
-    if (b_scale_mode != 0)
-        return 128;
     const int forced = g_tile_n.load(std::memory_order_relaxed);
+    if (b_scale_mode != 0) {
+        // Per-row B scales are built for the 128 and 256 widths only.
+        if (forced == 128 || forced == 256)
+            return forced;
+        return N > 128 ? 256 : 128;
+    }
     if (forced)
         return forced;
     if (N <= 128)

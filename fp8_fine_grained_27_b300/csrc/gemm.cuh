@@ -213,6 +213,23 @@ __device__ void build_tile_start(const Params &p, int *tile_start, int ptid)
         tile_start[p.G] = run;
 }
 
+// Per-row B scales: acc.{x,y} = fl32(sa * sb.{x,y}) * P.{x,y} + acc.{x,y},
+// each product and sum rounded exactly as the scalar mul and fmaf would be,
+// two columns per instruction.
+__device__ __forceinline__ void fold_rowscale2(float &a0, float &a1, uint64_t sa2, float sb0, float sb1, uint32_t p0,
+                                               uint32_t p1)
+{
+    uint64_t acc, sc2;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(a0), "f"(a1));
+    asm("{\n\t.reg .b64 t;\n\tmov.b64 t, {%1, %2};\n\tmul.rn.f32x2 %0, %3, t;\n\t}"
+        : "=l"(sc2)
+        : "f"(sb0), "f"(sb1), "l"(sa2));
+    asm("{\n\t.reg .b64 t;\n\tmov.b64 t, {%1, %2};\n\tfma.rn.f32x2 %0, %3, t, %0;\n\t}"
+        : "+l"(acc)
+        : "r"(p0), "r"(p1), "l"(sc2));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     uint32_t r;
@@ -450,13 +467,15 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                         for (int j = 0; j < 32; ++j)
                             acc[pc * 32 + j] = fmaf(sc, __uint_as_float(cur[j]), acc[pc * 32 + j]);
                     } else {
+                        uint64_t sa2;
+                        asm("mov.b64 %0, {%1, %1};" : "=l"(sa2) : "f"(sa_v));
 #pragma unroll
                         for (int j = 0; j < 32; j += 4) {
                             const float4 sb4 = *reinterpret_cast<const float4 *>(sbr + pc * 32 + j);
-                            acc[pc * 32 + j + 0] = fmaf(sa_v * sb4.x, __uint_as_float(cur[j + 0]), acc[pc * 32 + j + 0]);
-                            acc[pc * 32 + j + 1] = fmaf(sa_v * sb4.y, __uint_as_float(cur[j + 1]), acc[pc * 32 + j + 1]);
-                            acc[pc * 32 + j + 2] = fmaf(sa_v * sb4.z, __uint_as_float(cur[j + 2]), acc[pc * 32 + j + 2]);
-                            acc[pc * 32 + j + 3] = fmaf(sa_v * sb4.w, __uint_as_float(cur[j + 3]), acc[pc * 32 + j + 3]);
+                            fold_rowscale2(acc[pc * 32 + j + 0], acc[pc * 32 + j + 1], sa2, sb4.x, sb4.y, cur[j + 0],
+                                           cur[j + 1]);
+                            fold_rowscale2(acc[pc * 32 + j + 2], acc[pc * 32 + j + 3], sa2, sb4.z, sb4.w, cur[j + 2],
+                                           cur[j + 3]);
                         }
                     }
                 };

@@ -88,9 +88,16 @@ def _wgrad(fb, orc, dY, X, rows=None, what=""):
     return assert_gemm_close(got, ref, what)
 
 
-def test_wgrad_small_full(fb, orc):
+def test_wgrad_small_full(fb, orc, tile_n):
     d = synth.wgrad(T=1024, Cout=256, Cin=392)
     _wgrad(fb, orc, d["dY"], d["X"], what="wgrad small")
+
+
+@pytest.mark.parametrize("Cout,Cin,T", [(128, 8, 128), (384, 264, 384), (256, 136, 256)])
+def test_wgrad_ragged(fb, orc, tile_n, Cout, Cin, T):
+    """Per-row B scales on output widths that end inside a tile."""
+    d = synth.wgrad(T=T, Cout=Cout, Cin=Cin)
+    _wgrad(fb, orc, d["dY"], d["X"], what=f"wgrad {Cout}x{Cin}x{T}")
 
 
 def test_wgrad_full_size_sampled(fb, orc):
