@@ -145,6 +145,8 @@ def workload_desc(name):
                 "gemms": 1, "quant": "A 1x128, B 128x128", "out": "bf16"},
         "wgrad": {"workload": "wgrad", "M": 2048, "K": 16384, "N": [7168],
                   "gemms": 1, "quant": "dY, X 1x128 along tokens (transposed)", "out": "fp32"},
+        "dgrad": {"workload": "dgrad_ffn", "M": 16384, "K": 18432, "N": [7168], "gemms": 1,
+                  "quant": "dY 1x128, W 128x128 written transposed (codes + scales)", "out": "bf16"},
         "moe": {"workload": "moe_grouped_up", "M": 32768, "K": 7168, "N": [4096], "experts": 256,
                 "topk": 8, "gemms": 1, "quant": "grouped rows 1x128 (weights pre-quantised)", "out": "bf16"},
         "tiny": {"workload": "tiny", "M": 128, "K": 512, "N": [256], "gemms": 1,
@@ -168,6 +170,8 @@ def quant_bytes(name):
     if name == "wgrad":
         e = d["K"] * (d["M"] + d["N"][0])
         return e * (3 + 4 / 128)
+    if name == "dgrad":
+        return d["M"] * d["K"] * (3 + 4 / 128) + d["K"] * d["N"][0] * (3 + 4 / (128 * 128))
     if name == "moe":
         return d["M"] * d["K"] * (3 + 4 / 128)
     raise KeyError(name)
@@ -191,6 +195,9 @@ class Step:
         elif name == "wgrad":
             d = synth.wgrad(seed=seed)
             self.host = {"dY": d["dY"], "X": d["X"]}
+        elif name == "dgrad":
+            d = synth.dgrad(seed=seed)
+            self.host = {"dY": d["dY"], "W": d["W"]}
         elif name == "moe":
             tok = synth.moe_tokens(seed=seed)
             offs, token_of_row = synth.moe_route(tok, seed=seed)
@@ -215,6 +222,15 @@ class Step:
             self.d["qx"] = torch.empty((Ci, T), dtype=torch.uint8, device="cuda")
             self.d["sx"] = torch.empty((T // 128, Ci), dtype=torch.float32, device="cuda")
             self.d["C"] = [torch.empty((Co, Ci), dtype=torch.float32, device="cuda")]
+        elif name == "dgrad":
+            self.d["dY"], self.d["W"] = dev(self.host["dY"]), dev(self.host["W"])
+            T, Co = self.host["dY"].shape
+            Ci = self.host["W"].shape[1]
+            self.d["qdy"] = torch.empty((T, Co), dtype=torch.uint8, device="cuda")
+            self.d["sdy"] = torch.empty((Co // 128, T), dtype=torch.float32, device="cuda")
+            self.d["qwt"] = torch.empty((Ci, Co), dtype=torch.uint8, device="cuda")
+            self.d["swt"] = torch.empty((Ci // 128, (Co + 127) // 128), dtype=torch.float32, device="cuda")
+            self.d["C"] = [torch.empty((T, Ci), dtype=torch.bfloat16, device="cuda")]
         elif name == "moe":
             self.d["A"] = dev(self.host["A"])
             M, K = self.host["A"].shape
@@ -247,6 +263,10 @@ class Step:
             return [("quant_1x128_cols", lambda: fb.quant_1x128(d["dY"], along=1, q=d["qdy"], s=d["sdy"])),
                     ("quant_1x128_cols", lambda: fb.quant_1x128(d["X"], along=1, q=d["qx"], s=d["sx"])),
                     ("gemm", lambda: fb.gemm_blockscaled(d["qdy"], d["sdy"], d["qx"], d["sx"], 1, C=d["C"][0]))]
+        if self.name == "dgrad":
+            return [("quant_1x128", lambda: fb.quant_1x128(d["dY"], q=d["qdy"], s=d["sdy"])),
+                    ("quant_128x128_t", lambda: fb.quant_128x128_t(d["W"], straight=False, qt=d["qwt"], st=d["swt"])),
+                    ("gemm", lambda: fb.gemm_blockscaled(d["qdy"], d["sdy"], d["qwt"], d["swt"], 0, C=d["C"][0]))]
         if self.name == "moe":
             return [("quant_1x128", lambda: fb.quant_1x128(d["A"], q=d["qa"], s=d["sa"])),
                     ("gemm", lambda: fb.grouped_gemm_moe(d["qa"], d["sa"], d["qb"], d["sb"], d["offs"],
@@ -259,6 +279,8 @@ class Step:
             return [("A", self.host["A"])] + [(f"W{i}", w) for i, w in enumerate(self.host["W"])]
         if self.name == "wgrad":
             return [("dY", self.host["dY"]), ("X", self.host["X"])]
+        if self.name == "dgrad":
+            return [("dY", self.host["dY"]), ("W", self.host["W"])]
         return [("A", self.host["A"])]
 
 
@@ -393,6 +415,8 @@ def run_e2e(args, step, torch, fb, launches, flops, world, dist):
         targets = {"A": step.d["A"], **{f"W{i}": w for i, w in enumerate(step.d["W"])}}
     elif step.name == "wgrad":
         targets = {"dY": step.d["dY"], "X": step.d["X"]}
+    elif step.name == "dgrad":
+        targets = {"dY": step.d["dY"], "W": step.d["W"]}
     else:
         targets = {"A": step.d["A"]}
     h2d = sum(p.numel() * p.element_size() for _, p in pinned)
@@ -460,6 +484,15 @@ def oracle_sample(workload, seed=0):
             qx, sx = oracle.quant_1x128_cols(X)
             oracle.gemm_blockscaled(qd, sd, qx, sx, 1)
         return work, 2.0 * 16 * 512 * 16384, "16 x 512 outputs of dW (K = 16384 tokens), with their token-wise quantisation"
+    if workload == "dgrad":
+        d = synth.dgrad(seed=seed, T=16)
+        dY, W = d["dY"], np.ascontiguousarray(d["W"][:, :2048])
+
+        def work():
+            qd, sd = oracle.quant_1x128_rows(dY)
+            _, _, qwt, swt = oracle.quant_128x128_t(W)
+            oracle.gemm_blockscaled(qd, sd, qwt, swt, 0)
+        return work, 2.0 * 16 * 2048 * 18432, "16 rows x 2048 columns of dX (K = 18432), with their quantisation"
     if workload == "moe":
         tok = synth.moe_tokens(seed=seed, T=64)
         W = synth.moe_weights("up", 0, 1, seed=seed)[0][:1024]
@@ -521,7 +554,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
-    ap.add_argument("--workload", default="mla", choices=["mla", "ffn", "wgrad", "moe", "tiny"])
+    ap.add_argument("--workload", default="mla", choices=["mla", "ffn", "wgrad", "dgrad", "moe", "tiny"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
@@ -535,7 +568,7 @@ def main():
         args.warmup = args.warmup if args.warmup is not None else 1
         run_reference(args, rank, world)
         return
-    default_steps = {"mla": 10000, "tiny": 10000, "ffn": 200, "wgrad": 1000, "moe": 300}[args.workload]
+    default_steps = {"mla": 10000, "tiny": 10000, "ffn": 200, "wgrad": 1000, "dgrad": 200, "moe": 300}[args.workload]
     args.steps = args.steps or default_steps
     args.warmup = max(3, args.warmup if args.warmup is not None else 20)
     run_ours(args, rank, world)

@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     lib,
     quant_1x128,
     quant_128x128,
+    quant_128x128_t,
     selftest_division,
     selftest_timeout,
     set_gemm_tile_n,

@@ -19,8 +19,8 @@ OK, EINVAL, EALIGN, EARCH, ECUDA, ETIMEOUT = 0, -1, -2, -3, -4, -5
 
 # every symbol include/fp8bs.h declares
 EXPORTS = (
-    "fp8_quant_1x128", "fp8_quant_128x128", "fp8_gemm_blockscaled", "fp8_grouped_gemm_moe",
-    "fp8bs_e4m3_encode", "fp8bs_status_string", "fp8bs_get_device_error",
+    "fp8_quant_1x128", "fp8_quant_128x128", "fp8_quant_128x128_t", "fp8_gemm_blockscaled",
+    "fp8_grouped_gemm_moe", "fp8bs_e4m3_encode", "fp8bs_status_string", "fp8bs_get_device_error",
     "fp8bs_selftest_timeout", "fp8bs_selftest_division", "fp8bs_set_gemm_tile_n", "fp8bs_version",
 )
 
@@ -44,6 +44,7 @@ def lib() -> ctypes.CDLL:
         i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
         L.fp8_quant_1x128.argtypes = [vp, i64, i64, i64, i32, vp, i64, vp, i64, vp]
         L.fp8_quant_128x128.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp]
+        L.fp8_quant_128x128_t.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp]
         L.fp8_gemm_blockscaled.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i32, vp, i64, i32, i64, i64, i64, vp]
         L.fp8_grouped_gemm_moe.argtypes = [vp, i64, vp, i64, vp, vp, vp, i32, i64, vp, i64, i32, i64, i64, vp]
         L.fp8bs_e4m3_encode.argtypes = [vp, vp, i64, vp]
@@ -54,7 +55,7 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_selftest_division.argtypes = [vp, vp]
         L.fp8bs_set_gemm_tile_n.argtypes = [i32]
         L.fp8bs_version.restype = ctypes.c_char_p
-        for name in ("fp8_quant_1x128", "fp8_quant_128x128", "fp8_gemm_blockscaled",
+        for name in ("fp8_quant_1x128", "fp8_quant_128x128", "fp8_quant_128x128_t", "fp8_gemm_blockscaled",
                      "fp8_grouped_gemm_moe", "fp8bs_e4m3_encode", "fp8bs_get_device_error",
                      "fp8bs_selftest_timeout", "fp8bs_selftest_division", "fp8bs_set_gemm_tile_n"):
             getattr(L, name).restype = i32
@@ -104,6 +105,26 @@ def quant_128x128(w: torch.Tensor, q=None, s=None, stream=None):
     _check("fp8_quant_128x128", lib().fp8_quant_128x128(_ptr(w), N, K, _ld(w), _ptr(q), _ld(q),
                                                         _ptr(s), _ld(s), _stream(stream)))
     return q, s
+
+
+def quant_128x128_t(w: torch.Tensor, straight: bool = True, q=None, s=None, qt=None, st=None, stream=None):
+    """128x128 block quantisation of BF16 w [N, K] with transposed outputs:
+    qt [K, N] codes and st [K/128, ceil(N/128)] scales (the quantisation of w^T), plus, when
+    straight, q [N, K] and s [ceil(N/128), K/128] as quant_128x128 writes them.
+    Returns (q, s, qt, st); q and s are None when not straight."""
+    N, K = w.shape
+    nb = (N + 127) // 128
+    if straight:
+        q = torch.empty((N, K), dtype=torch.uint8, device=w.device) if q is None else q
+        s = torch.empty((nb, K // 128), dtype=torch.float32, device=w.device) if s is None else s
+    else:
+        q = s = None
+    qt = torch.empty((K, N), dtype=torch.uint8, device=w.device) if qt is None else qt
+    st = torch.empty((K // 128, nb), dtype=torch.float32, device=w.device) if st is None else st
+    _check("fp8_quant_128x128_t", lib().fp8_quant_128x128_t(
+        _ptr(w), N, K, _ld(w), _ptr(q), _ld(q) if q is not None else 0, _ptr(s), _ld(s) if s is not None else 0,
+        _ptr(qt), _ld(qt), _ptr(st), _ld(st), _stream(stream)))
+    return q, s, qt, st
 
 
 def gemm_blockscaled(A, sa, B, sb, b_scale_mode: int = 0, out_dtype=torch.bfloat16, C=None, stream=None):

@@ -41,6 +41,7 @@ struct DeviceInfo {
     int quant_rows_ctas = 0;  // resident CTAs per SM, 1x128 and 128x128 kernels
     int quant_block_ctas = 0;
     int quant_cols_ctas = 0;
+    int quant_blockt_ctas = 0;
     unsigned gemm_attr_set = 0;  // bit per GEMM instance: shared-memory attribute applied
 };
 
@@ -74,10 +75,10 @@ int current_device(DeviceInfo **out)
                 cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.quant_block_ctas, quant::quant_rows_kernel<true>,
                                                               quant::kThreads, 0) != cudaSuccess)
                 return FP8BS_ECUDA;
-            if (cudaFuncSetAttribute(quant::quant_cols_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     sizeof(quant::ColsSmem)) != cudaSuccess ||
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.quant_cols_ctas, quant::quant_cols_kernel,
-                                                              quant::kThreads, sizeof(quant::ColsSmem)) != cudaSuccess)
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.quant_cols_ctas, quant::quant_t_kernel<false>,
+                                                              quant::kThreads, 0) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.quant_blockt_ctas, quant::quant_t_kernel<true>,
+                                                              quant::kThreads, 0) != cudaSuccess)
                 return FP8BS_ECUDA;
             if (!g_encode) {
                 void *fn = nullptr;
@@ -231,8 +232,8 @@ int fp8_quant_1x128(const void *x, int64_t M, int64_t K, int64_t ldx, int along,
             return FP8BS_EINVAL;
         const int64_t tiles = (M / 128) * ((K + 127) / 128);
         const int64_t grid = std::min<int64_t>(tiles, int64_t(d->num_sms) * d->quant_cols_ctas);
-        quant::quant_cols_kernel<<<static_cast<int>(grid), quant::kThreads, sizeof(quant::ColsSmem), st>>>(
-            static_cast<const uint16_t *>(x), M, K, ldx, q, ldq, s, lds);
+        quant::quant_t_kernel<false><<<static_cast<int>(grid), quant::kThreads, 0, st>>>(
+            static_cast<const uint16_t *>(x), M, K, ldx, nullptr, 0, q, ldq, s, lds, nullptr, 0);
     }
     return launch_status();
 }
@@ -258,6 +259,35 @@ int fp8_quant_128x128(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t 
     const int64_t grid = std::min<int64_t>(tiles, int64_t(d->num_sms) * d->quant_block_ctas);
     quant::quant_rows_kernel<true><<<static_cast<int>(grid), quant::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t *>(w), N, K, ldw, q, ldq, s, lds);
+    return launch_status();
+}
+
+int fp8_quant_128x128_t(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq, float *s,
+                        int64_t lds, uint8_t *qt, int64_t ldqt, float *st, int64_t ldst, void *stream)
+{
+    if (N < 0 || K < 0)
+        return FP8BS_EINVAL;
+    if (N == 0 || K == 0)
+        return FP8BS_OK;
+    if (!w || !qt || !st || (q == nullptr) != (s == nullptr))
+        return FP8BS_EINVAL;
+    if (ldw < K || K % 128 != 0 || N % 16 != 0 || ldqt < N || ldst < (N + 127) / 128)
+        return FP8BS_EINVAL;
+    if (q && (ldq < K || lds < K / 128))
+        return FP8BS_EINVAL;
+    if (N > (int64_t(1) << 31) || K > (int64_t(1) << 31))
+        return FP8BS_EINVAL;
+    if (!aligned16(w) || !aligned16(qt) || (ldw * 2) % 16 != 0 || ldqt % 16 != 0 ||
+        (q && (!aligned16(q) || ldq % 16 != 0)))
+        return FP8BS_EALIGN;
+    DeviceInfo *d;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK)
+        return rc;
+    const int64_t tiles = ((N + 127) / 128) * (K / 128);
+    const int64_t grid = std::min<int64_t>(tiles, int64_t(d->num_sms) * d->quant_blockt_ctas);
+    quant::quant_t_kernel<true><<<static_cast<int>(grid), quant::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(w), N, K, ldw, q, ldq, qt, ldqt, s, lds, st, ldst);
     return launch_status();
 }
 

@@ -21,17 +21,26 @@ constexpr int kThreads = 256;
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// max of the magnitudes held in a 16-byte group of 8 BF16 values, as a pair
-// of 16-bit lanes (sign bits cleared).
+// Magnitude maximum of two BF16 pairs, lane-wise: the magnitude of each lane
+// of the result is max(|a|, |b|) (its sign bit is meaningless, clear it with
+// 0x7FFF7FFF before use).  One instruction per pair, exact for every finite
+// input including subnormals.
+__device__ __forceinline__ uint32_t absmax2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// magnitude maximum of the 8 BF16 values of a 16-byte group, as a pair (signs unspecified)
 __device__ __forceinline__ uint32_t amax8(const uint4 &v)
 {
-    uint32_t a = __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
-    uint32_t b = __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu);
-    return __vmaxu2(a, b);
+    return absmax2(absmax2(v.x, v.y), absmax2(v.z, v.w));
 }
 
 __device__ __forceinline__ float pair_max_to_f32(uint32_t m2)
 {
+    m2 &= 0x7FFF7FFFu;
     uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
     return __uint_as_float(m << 16);
 }
@@ -50,9 +59,13 @@ __device__ __forceinline__ float tile_scale(float amax)
 // q can differ from the IEEE quotient in its last bit (near underflow), but
 // its E4M3 code never does: fp8bs_selftest_division encodes both for every
 // BF16 amax and every BF16 x with |x| <= amax (about 2^31 pairs) and finds no
-// difference.  The low and high value may have different scales (two
-// columns of the transposed quantiser).  Scales below 2^-100 (reciprocal
-// near overflow) take the IEEE divide.
+// difference.  (RN(x r) alone is not enough: its codes differ for about 3e4
+// of those pairs.)  The one value whose sign the correction step loses is
+// x = -0 (q = +0); the callers OR the input sign bits into the codes
+// (signs4), which restores it and changes no other code, since every other
+// quotient already carries x's sign.  The low and high value may have
+// different scales (two columns of the transposed quantiser).  Scales below
+// 2^-100 (reciprocal near overflow) take the IEEE divide instead.
 __device__ __forceinline__ uint64_t pack2(float lo, float hi)
 {
     uint64_t r;
@@ -65,39 +78,26 @@ __device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi)
     asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
 }
 
-struct QuotientPair {
+__device__ __forceinline__ bool markstein_ok(float s) { return s >= 0x1p-100f; }
+
+struct Markstein2 {
     uint64_t r2, ns2;
-    float s_lo, s_hi;
-    bool fast;
-    __device__ __forceinline__ QuotientPair(float scale_lo, float scale_hi)
+    __device__ __forceinline__ Markstein2(float s_lo, float s_hi)
     {
-        s_lo = scale_lo;
-        s_hi = scale_hi;
-        fast = scale_lo >= 0x1p-100f && scale_hi >= 0x1p-100f;
-        r2 = pack2(__frcp_rn(scale_lo), __frcp_rn(scale_hi));
-        ns2 = pack2(-scale_lo, -scale_hi);
+        r2 = pack2(__frcp_rn(s_lo), __frcp_rn(s_hi));
+        ns2 = pack2(-s_lo, -s_hi);
     }
     // quotients of the two values of BF16 pair word w (low half first)
     __device__ __forceinline__ void quot(uint32_t w, float &q_lo, float &q_hi) const
     {
-        const float x_lo = bf16lo(w), x_hi = bf16hi(w);
-        if (fast) {
-            const uint64_t x2 = pack2(x_lo, x_hi);
-            uint64_t q0, e, q;
-            asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(x2), "l"(r2));
-            asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(q0), "l"(ns2), "l"(x2));
-            asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(e), "l"(r2), "l"(q0));
-            unpack2(q, q_lo, q_hi);
-            // s > 0, so a quotient carries x's sign; the correction step
-            // would turn -0 into +0, so the sign is restored explicitly
-            q_lo = copysignf(q_lo, x_lo);
-            q_hi = copysignf(q_hi, x_hi);
-        } else {
-            q_lo = __fdiv_rn(x_lo, s_lo);
-            q_hi = __fdiv_rn(x_hi, s_hi);
-        }
+        const uint64_t x2 = pack2(bf16lo(w), bf16hi(w));
+        uint64_t q0, e, q;
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(x2), "l"(r2));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(q0), "l"(ns2), "l"(x2));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(e), "l"(r2), "l"(q0));
+        unpack2(q, q_lo, q_hi);
     }
-    // E4M3 codes of the pair: low value in the low byte
+    // E4M3 codes of the pair, low value in the low byte (a -0 input gives 0x00)
     __device__ __forceinline__ uint32_t codes(uint32_t w) const
     {
         float lo, hi;
@@ -105,6 +105,25 @@ struct QuotientPair {
         return e4m3x2(lo, hi);
     }
 };
+
+// codes of BF16 pair word w by the IEEE divide (scales below 2^-100)
+__device__ __forceinline__ uint32_t codes_ieee(uint32_t w, float s_lo, float s_hi)
+{
+    return e4m3x2(__fdiv_rn(bf16lo(w), s_lo), __fdiv_rn(bf16hi(w), s_hi));
+}
+
+// the sign bits of the four BF16 values of w0 (values 0, 1) and w1 (values
+// 2, 3), at bit 7 of bytes 0 .. 3
+__device__ __forceinline__ uint32_t signs4(uint32_t w0, uint32_t w1)
+{
+    return __byte_perm(w0, w1, 0x7531) & 0x80808080u;
+}
+
+// four codes (bytes 0 .. 3) from two 16-bit code pairs and the input words
+__device__ __forceinline__ uint32_t join4(uint32_t c0, uint32_t c1, uint32_t w0, uint32_t w1)
+{
+    return __byte_perm(c0, c1, 0x5410) | signs4(w0, w1);
+}
 
 __device__ __forceinline__ uint4 ldg_stream(const void *p)
 {
@@ -157,28 +176,28 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t *__
         uint32_t am[2];
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr)
-            am[rr] = __vmaxu2(__vmaxu2(amax8(v[rr][0]), amax8(v[rr][1])), __vmaxu2(amax8(v[rr][2]), amax8(v[rr][3])));
+            am[rr] = absmax2(absmax2(amax8(v[rr][0]), amax8(v[rr][1])), absmax2(amax8(v[rr][2]), amax8(v[rr][3])));
         float sc[2];
         if constexpr (!kBlock) {
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
                 uint32_t a = am[rr];
-                a = __vmaxu2(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-                a = __vmaxu2(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+                a = absmax2(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+                a = absmax2(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
                 sc[rr] = tile_scale(pair_max_to_f32(a));
             }
         } else {
-            uint32_t a = __vmaxu2(am[0], am[1]);
+            uint32_t a = absmax2(am[0], am[1]);
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1)
-                a = __vmaxu2(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+                a = absmax2(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
             if (lane == 0)
                 red[tid >> 5] = a;
             __syncthreads();
             uint32_t b = red[0];
 #pragma unroll
             for (int w = 1; w < kThreads / 32; ++w)
-                b = __vmaxu2(b, red[w]);
+                b = absmax2(b, red[w]);
             sc[0] = sc[1] = tile_scale(pair_max_to_f32(b));
             __syncthreads();  // red[] is rewritten by the next tile
         }
@@ -186,14 +205,27 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t *__
         for (int rr = 0; rr < 2; ++rr) {
             const int64_t m = m0 + rw + 64 * rr;
             if (m < M) {
-                const QuotientPair qt(sc[rr], sc[rr]);
+                uint2 c[4];
+                if (markstein_ok(sc[rr])) {
+                    const Markstein2 d(sc[rr], sc[rr]);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    uint2 c;
-                    c.x = qt.codes(v[rr][i].x) | (qt.codes(v[rr][i].y) << 16);
-                    c.y = qt.codes(v[rr][i].z) | (qt.codes(v[rr][i].w) << 16);
-                    *reinterpret_cast<uint2 *>(q + m * ldq + kb * 128 + (j + 4 * i) * 8) = c;
+                    for (int i = 0; i < 4; ++i) {
+                        const uint4 &x = v[rr][i];
+                        c[i].x = join4(d.codes(x.x), d.codes(x.y), x.x, x.y);
+                        c[i].y = join4(d.codes(x.z), d.codes(x.w), x.z, x.w);
+                    }
+                } else {
+                    const float sv = sc[rr];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint4 &x = v[rr][i];
+                        c[i].x = join4(codes_ieee(x.x, sv, sv), codes_ieee(x.y, sv, sv), x.x, x.y);
+                        c[i].y = join4(codes_ieee(x.z, sv, sv), codes_ieee(x.w, sv, sv), x.z, x.w);
+                    }
                 }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    *reinterpret_cast<uint2 *>(q + m * ldq + kb * 128 + (j + 4 * i) * 8) = c[i];
                 if (!kBlock && j == 0)
                     s[kb * lds + m] = sc[rr];
             }
@@ -204,140 +236,216 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t *__
 }
 
 // ---------------------------------------------------------------------------
-// Tiles of 128 consecutive rows of one column (the token dimension of a
-// weight-gradient operand), codes written transposed.  A CTA stages a
-// 128-row x 128-column BF16 tile in shared memory (row pitch 65 words: the
-// column reads of 32 consecutive rows hit 32 distinct banks), reduces each
-// column, encodes into a [128 columns][128 rows] byte tile and writes it out
-// with 16-byte coalesced stores.
-//   x [T][ldx] (C columns); q [C][ldq] (row k holds the T codes of column k);
-//   s [T/128][lds]: scale of tile (tb, k) at s[tb*lds + k].
+// Tiles whose codes come out transposed.  A CTA takes 128 rows x 128
+// contiguous columns of x [R][ldx]; a thread holds two 4-row x 8-column
+// pieces (rows 4g .. 4g+3 for g = its row group and g + 16), read with
+// 16-byte loads (each warp instruction reads two full 256-byte row
+// segments).  Its codes are transposed in registers (byte permutes: one
+// 32-bit word = 4 consecutive rows of one column) and stored as words into a
+// [128 columns][32 words] shared tile whose word index is XOR-swizzled with
+// twice the column's 8-group, so that every store and every 16-byte read is
+// free of bank conflicts; the tile then leaves as 128-byte row segments of
+// qt [C][ldqt] (qt[c*ldqt + r] is the code of x[r][c]).
+//   kBlock = false: one scale per column per 128 rows (the 1x128 tiles of a
+//                   weight-gradient operand, which run along tokens);
+//                   s[rb*lds + c].
+//   kBlock = true : one scale per 128x128 block (weights), also written
+//                   transposed: s[rb*lds + cb] (may be null) and
+//                   st[cb*ldst + rb]; q [R][ldq] receives the untransposed
+//                   codes too unless null.
+// Rows past R (kBlock, R % 16 == 0) and 8-column groups past C are read as
+// zeros and never written.
 // ---------------------------------------------------------------------------
-constexpr int kColsPitch = 65;  // words per staged row (64 data words + 1)
-
-struct ColsSmem {
-    uint32_t xs[128 * kColsPitch];
-    uint8_t qs[128 * 128];
-    uint32_t red[4][64];
-    float sc[128];
-};
-
-__global__ void __launch_bounds__(kThreads) quant_cols_kernel(const uint16_t *__restrict__ x, int64_t T,
-                                                              int64_t C, int64_t ldx,
-                                                              uint8_t *__restrict__ q, int64_t ldq,
-                                                              float *__restrict__ s, int64_t lds)
+__device__ __forceinline__ void transpose4x4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t out[4])
 {
-    extern __shared__ __align__(16) uint8_t dyn_smem[];
-    ColsSmem &sm = *reinterpret_cast<ColsSmem *>(dyn_smem);
+    // a_i holds row i, byte j = column j; out[j] holds column j, byte i = row i
+    const uint32_t t0 = __byte_perm(a0, a1, 0x5140), t1 = __byte_perm(a2, a3, 0x5140);
+    const uint32_t t2 = __byte_perm(a0, a1, 0x7362), t3 = __byte_perm(a2, a3, 0x7362);
+    out[0] = __byte_perm(t0, t1, 0x5410);
+    out[1] = __byte_perm(t0, t1, 0x7632);
+    out[2] = __byte_perm(t2, t3, 0x5410);
+    out[3] = __byte_perm(t2, t3, 0x7632);
+}
+
+template <bool kBlock>
+__global__ void __launch_bounds__(kThreads, 4) quant_t_kernel(const uint16_t *__restrict__ x, int64_t R, int64_t C,
+                                                           int64_t ldx, uint8_t *__restrict__ q, int64_t ldq,
+                                                           uint8_t *__restrict__ qt, int64_t ldqt,
+                                                           float *__restrict__ s, int64_t lds,
+                                                           float *__restrict__ st, int64_t ldst)
+{
+    __shared__ __align__(16) uint32_t qs[128 * 32];
+    __shared__ __align__(16) uint4 red[kThreads / 32][16];
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    const int64_t ntb = T / 128;
-    const int64_t ncb = (C + 127) / 128;
-    const int64_t ntiles = ntb * ncb;
+    const int cg = lane & 15;                   // 8-column group of the tile
+    const int g0 = warp * 2 + (lane >> 4);      // 4-row group (and g0 + 16)
+    const int64_t nrb = (R + 127) / 128, ncb = (C + 127) / 128;
+    const int64_t ntiles = nrb * ncb;
 
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-        const int64_t cb = tile % ncb;
-        const int64_t tb = tile / ncb;
-        const int64_t t0 = tb * 128, c0 = cb * 128;
-
-        // 1. load 128 rows x 256 bytes, 16 bytes per thread per row
-        {
-            const int c16 = tid & 15;
-            const int rr = tid >> 4;
-            uint4 v[8];
-            const bool colok = c0 + c16 * 8 < C;
+        const int64_t cb = tile % ncb, rb = tile / ncb;
+        const int64_t r0 = rb * 128, c0 = cb * 128;
+        const bool colok = c0 + cg * 8 < C;
+        uint4 v[2][4];
 #pragma unroll
-            for (int p = 0; p < 8; ++p) {
-                const int64_t t = t0 + rr + 16 * p;
-                v[p] = colok ? ldg_stream(x + t * ldx + c0 + c16 * 8) : make_uint4(0, 0, 0, 0);
-            }
+        for (int u = 0; u < 2; ++u)
 #pragma unroll
-            for (int p = 0; p < 8; ++p) {
-                uint32_t *dst = &sm.xs[(rr + 16 * p) * kColsPitch + c16 * 4];
-                dst[0] = v[p].x;
-                dst[1] = v[p].y;
-                dst[2] = v[p].z;
-                dst[3] = v[p].w;
+            for (int i = 0; i < 4; ++i) {
+                const int64_t r = r0 + (g0 + 16 * u) * 4 + i;
+                v[u][i] = (colok && r < R) ? ldg_stream(x + r * ldx + c0 + cg * 8) : make_uint4(0, 0, 0, 0);
             }
-        }
-        __syncthreads();
 
-        // 2. column amax: thread -> word column w (2 columns), quarter of the rows
-        {
-            const int w = tid & 63;
-            const int qr = tid >> 6;
-            uint32_t a = 0;
-#pragma unroll 8
-            for (int r = 0; r < 32; ++r)
-                a = __vmaxu2(a, sm.xs[(qr * 32 + r) * kColsPitch + w] & 0x7FFF7FFFu);
-            sm.red[qr][w] = a;
-        }
-        __syncthreads();
-        if (tid < 64) {
-            uint32_t a = __vmaxu2(__vmaxu2(sm.red[0][tid], sm.red[1][tid]),
-                                  __vmaxu2(sm.red[2][tid], sm.red[3][tid]));
-            const float slo = tile_scale(__uint_as_float((a & 0xFFFFu) << 16));
-            const float shi = tile_scale(__uint_as_float(a & 0xFFFF0000u));
-            sm.sc[2 * tid] = slo;
-            sm.sc[2 * tid + 1] = shi;
-            if (c0 + 2 * tid < C) {
-                s[tb * lds + c0 + 2 * tid] = slo;
-                s[tb * lds + c0 + 2 * tid + 1] = shi;
-            }
-        }
-        __syncthreads();
-
-        // 3. encode: warp -> 8 word columns; lane -> rows lane + 32j
-#pragma unroll 1
-        for (int i = 0; i < 8; ++i) {
-            const int w = warp * 8 + i;
-            const QuotientPair qp(sm.sc[2 * w], sm.sc[2 * w + 1]);
+        // magnitude maximum of each column pair over this thread's 8 rows
+        uint4 m4 = v[0][0];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int r = lane + 32 * j;
-                const uint32_t word = sm.xs[r * kColsPitch + w];
-                const uint32_t c2 = qp.codes(word);
-                sm.qs[(2 * w) * 128 + r] = static_cast<uint8_t>(c2 & 0xFF);
-                sm.qs[(2 * w + 1) * 128 + r] = static_cast<uint8_t>(c2 >> 8);
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int i = (u == 0 ? 1 : 0); i < 4; ++i) {
+                m4.x = absmax2(m4.x, v[u][i].x);
+                m4.y = absmax2(m4.y, v[u][i].y);
+                m4.z = absmax2(m4.z, v[u][i].z);
+                m4.w = absmax2(m4.w, v[u][i].w);
             }
+        float sc[8];
+        if constexpr (!kBlock) {
+            m4.x = absmax2(m4.x, __shfl_xor_sync(0xFFFFFFFFu, m4.x, 16));
+            m4.y = absmax2(m4.y, __shfl_xor_sync(0xFFFFFFFFu, m4.y, 16));
+            m4.z = absmax2(m4.z, __shfl_xor_sync(0xFFFFFFFFu, m4.z, 16));
+            m4.w = absmax2(m4.w, __shfl_xor_sync(0xFFFFFFFFu, m4.w, 16));
+            if (lane < 16)
+                red[warp][cg] = m4;
+            __syncthreads();
+#pragma unroll
+            for (int w = 0; w < kThreads / 32; ++w) {
+                const uint4 o = red[w][cg];
+                m4.x = absmax2(m4.x, o.x);
+                m4.y = absmax2(m4.y, o.y);
+                m4.z = absmax2(m4.z, o.z);
+                m4.w = absmax2(m4.w, o.w);
+            }
+            const uint32_t mw[4] = {m4.x & 0x7FFF7FFFu, m4.y & 0x7FFF7FFFu, m4.z & 0x7FFF7FFFu, m4.w & 0x7FFF7FFFu};
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                sc[2 * p] = tile_scale(__uint_as_float((mw[p] & 0xFFFFu) << 16));
+                sc[2 * p + 1] = tile_scale(__uint_as_float(mw[p] & 0xFFFF0000u));
+            }
+            if (g0 == 0 && colok) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    s[rb * lds + c0 + cg * 8 + j] = sc[j];
+            }
+        } else {
+            uint32_t a = absmax2(absmax2(m4.x, m4.y), absmax2(m4.z, m4.w));
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1)
+                a = absmax2(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+            if (lane == 0)
+                red[warp][0].x = a;
+            __syncthreads();
+            uint32_t b = red[0][0].x;
+#pragma unroll
+            for (int w = 1; w < kThreads / 32; ++w)
+                b = absmax2(b, red[w][0].x);
+            const float sb = tile_scale(pair_max_to_f32(b));
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                sc[j] = sb;
+            if (tid == 0) {
+                if (s)
+                    s[rb * lds + cb] = sb;
+                st[cb * ldst + rb] = sb;
+            }
+        }
+
+        // codes; straight rows out, transposed words into the shared tile
+        uint32_t lo[2][4], hi[2][4];
+        float smin = sc[0];
+#pragma unroll
+        for (int j = 1; j < 8; ++j)
+            smin = fminf(smin, sc[j]);
+        if (markstein_ok(smin)) {
+            const Markstein2 d0(sc[0], sc[1]), d1(sc[2], sc[3]), d2(sc[4], sc[5]), d3(sc[6], sc[7]);
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 &x = v[u][i];
+                    lo[u][i] = join4(d0.codes(x.x), d1.codes(x.y), x.x, x.y);
+                    hi[u][i] = join4(d2.codes(x.z), d3.codes(x.w), x.z, x.w);
+                }
+        } else {
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 &x = v[u][i];
+                    lo[u][i] = join4(codes_ieee(x.x, sc[0], sc[1]), codes_ieee(x.y, sc[2], sc[3]), x.x, x.y);
+                    hi[u][i] = join4(codes_ieee(x.z, sc[4], sc[5]), codes_ieee(x.w, sc[6], sc[7]), x.z, x.w);
+                }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int g = g0 + 16 * u;
+            if (kBlock && q != nullptr && colok) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int64_t r = r0 + g * 4 + i;
+                    if (r < R)
+                        *reinterpret_cast<uint2 *>(q + r * ldq + c0 + cg * 8) = make_uint2(lo[u][i], hi[u][i]);
+                }
+            }
+            uint32_t cw[8];
+            transpose4x4(lo[u][0], lo[u][1], lo[u][2], lo[u][3], cw);
+            transpose4x4(hi[u][0], hi[u][1], hi[u][2], hi[u][3], cw + 4);
+            const int wsw = g ^ (2 * cg);
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc)
+                qs[(cg * 8 + cc) * 32 + wsw] = cw[cc];
         }
         __syncthreads();
 
-        // 4. write the transposed code tile: 128 rows x 8 chunks of 16 bytes
+        // transposed tile out: 128 columns x 8 chunks of 16 rows
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int idx = tid + kThreads * i;
-            const int row = idx >> 3, ch = idx & 7;
-            if (c0 + row < C) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(&sm.qs[row * 128 + ch * 16]);
-                *reinterpret_cast<uint4 *>(q + (c0 + row) * ldq + t0 + ch * 16) = v;
-            }
+            const int c = idx >> 3, ch = idx & 7;
+            const int f = 2 * (c >> 3);
+            uint4 w4 = *reinterpret_cast<const uint4 *>(&qs[c * 32 + ((4 * ch) ^ (f & 28))]);
+            if (f & 2)
+                w4 = make_uint4(w4.z, w4.w, w4.x, w4.y);
+            if (c0 + c < C && r0 + ch * 16 < R)
+                *reinterpret_cast<uint4 *>(qt + (c0 + c) * ldqt + r0 + ch * 16) = w4;
         }
-        __syncthreads();
     }
 }
 
-// Exhaustive check of QuotientPair against the IEEE divide over the whole
+// Exhaustive check of the quantisers' division (Markstein2 + signs4) against the IEEE divide over the whole
 // BF16 domain of the quantisers: block = one positive finite BF16 amax
 // (0x0001 .. 0x7F7F), threads = every BF16 x with |x| <= amax, both signs
 // (x and -x form one pair word).  counts[0] += values whose E4M3 codes
-// differ, counts[1] += values whose single-precision quotients differ.
+// differ, counts[1] += values whose single-precision quotients differ in
+// value (Markstein path only; -0 and +0 count as equal).
 __global__ void selftest_division_kernel(unsigned long long *counts)
 {
     const uint32_t abits = blockIdx.x + 1;  // 0x0001 .. 0x7F7F
     const float amax = __uint_as_float(abits << 16);
     const float s = tile_scale(amax);
-    const QuotientPair qp(s, s);
+    const bool fast = markstein_ok(s);
+    const Markstein2 d(s, s);
     unsigned long long bad_code = 0, bad_quot = 0;
     for (uint32_t xb = threadIdx.x; xb <= abits; xb += blockDim.x) {
         const uint32_t w = xb | ((xb | 0x8000u) << 16);  // low: +x, high: -x
-        float q_lo, q_hi;
-        qp.quot(w, q_lo, q_hi);
-        const uint32_t codes = qp.codes(w);
         const float i_lo = __fdiv_rn(bf16lo(w), s), i_hi = __fdiv_rn(bf16hi(w), s);
         const uint32_t icodes = e4m3x2(i_lo, i_hi);
-        bad_quot += (__float_as_uint(q_lo) != __float_as_uint(i_lo)) + (__float_as_uint(q_hi) != __float_as_uint(i_hi));
+        // the quantisers' path: Markstein + sign bits, or the IEEE divide
+        const uint32_t codes = (fast ? d.codes(w) : codes_ieee(w, s, s)) | (signs4(w, 0) & 0xFFFFu);
+        if (fast) {
+            float q_lo, q_hi;
+            d.quot(w, q_lo, q_hi);
+            bad_quot += (q_lo != i_lo) + (q_hi != i_hi);
+        }
         bad_code += ((codes & 0xFF) != (icodes & 0xFF)) + ((codes >> 8) != (icodes >> 8));
     }
     for (int o = 16; o >= 1; o >>= 1) {

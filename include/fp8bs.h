@@ -85,6 +85,27 @@ int fp8_quant_128x128(const void *w, int64_t N, int64_t K, int64_t ldw,
                       uint8_t *q, int64_t ldq, float *s, int64_t lds, void *stream);
 
 /*
+ * fp8_quant_128x128_t -- per-block 128x128 quantisation of a BF16 weight
+ * matrix that also writes the codes and block scales transposed, for the
+ * Dgrad GEMM (V3 report §6: Dgrad takes the FP8 weights; §6.1: 128x128
+ * weight blocks).  A 128x128 block is the same set of elements in W and in
+ * W^T, so the transposed codes and scales are exactly the quantisation of
+ * W^T: with them, dX = dY * W is fp8_gemm_blockscaled with A = codes of dY
+ * (1x128 along its channels) and B = W^T codes, b_scale_mode 0.
+ *   w   BF16 [N][ldw], K columns used (N = output channels of the layer).
+ *   q   codes [N][ldq] and s FP32 [ceil(N/128)][lds] exactly as
+ *       fp8_quant_128x128 writes them; both NULL to skip them.
+ *   qt  codes [K][ldqt], ldqt >= N: qt[k*ldqt + n] = code of w[n][k].
+ *   st  FP32 [K/128][ldst], ldst >= ceil(N/128): scale of block (nb, kb) at
+ *       st[kb*ldst + nb].
+ *   Requires K % 128 == 0 and N % 16 == 0; a partial last block row takes
+ *   its amax over the rows that exist.  One pass over w.
+ */
+int fp8_quant_128x128_t(const void *w, int64_t N, int64_t K, int64_t ldw,
+                        uint8_t *q, int64_t ldq, float *s, int64_t lds,
+                        uint8_t *qt, int64_t ldqt, float *st, int64_t ldst, void *stream);
+
+/*
  * fp8_gemm_blockscaled -- C = A * B^T from E4M3 codes with fine-grained
  * scales and FP32 promotion every 128 K (V3 report §6, §6.2).
  *
@@ -138,10 +159,12 @@ int fp8bs_e4m3_encode(const float *x, uint8_t *q, int64_t n, void *stream);
 /*
  * fp8bs_selftest_division -- the quantisers divide by the tile scale with a
  * per-tile reciprocal and one Markstein correction instead of an IEEE divide.
- * This diagnostic encodes both quotients to E4M3 for every positive finite
- * BF16 amax and every BF16 x with |x| <= amax (about 2^31 pairs) and writes
- * counts[0] = pairs whose codes differ (0 means the fast path is bit-exact on
- * every BF16 input), counts[1] = pairs whose FP32 quotients differ.
+ * This diagnostic encodes both quotients to E4M3 (the fast one with the
+ * quantisers' sign restoration for -0) for every positive finite BF16 amax
+ * and every BF16 x with |x| <= amax (about 2^31 values of each sign) and
+ * writes counts[0] = values whose codes differ (0 means the fast path is
+ * bit-exact on every BF16 input), counts[1] = values whose FP32 quotients
+ * differ in value.
  * counts: DEVICE unsigned long long [2].
  */
 int fp8bs_selftest_division(unsigned long long *counts, void *stream);

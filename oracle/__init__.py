@@ -162,6 +162,16 @@ def quant_128x128(w_bf16: np.ndarray, threads: int | None = None):
     return q, s
 
 
+def quant_128x128_t(w_bf16: np.ndarray, threads: int | None = None):
+    """128x128 block quantisation of w [N, K] and its transposed form (V3 report §6: the Dgrad GEMM
+    takes the FP8 weights; §6.1: 128x128 blocks).  A block of w^T holds the same elements as the
+    block of w it comes from, so its amax, scale and codes are the same: the transposed
+    quantisation is the transpose of the codes and of the block-scale grid.
+    Returns q [N, K], s [ceil(N/128), K/128], qt [K, N], st [K/128, ceil(N/128)]."""
+    q, s = quant_128x128(w_bf16, threads)
+    return q, s, np.ascontiguousarray(q.T), np.ascontiguousarray(s.T)
+
+
 # --- GEMM -------------------------------------------------------------------
 
 def gemm_blockscaled(A: np.ndarray, sa: np.ndarray, B: np.ndarray, sb: np.ndarray,

@@ -108,7 +108,7 @@ def bf16_to_f32(x: np.ndarray) -> np.ndarray:
 
 # --- workloads --------------------------------------------------------------
 
-WORKLOADS = {1: "tiny", 2: "mla", 3: "moe", 4: "wgrad", 5: "ffn"}
+WORKLOADS = {1: "tiny", 2: "mla", 3: "moe", 4: "wgrad", 5: "ffn", 6: "dgrad"}
 
 
 def tiny(seed: int = 0, M: int = 128, N: int = 256, K: int = 512):
@@ -141,6 +141,15 @@ def ffn(seed: int = 0, M: int = 16384, N: int = 18432, K: int = 7168):
 
 
 # MoE (workload 3) ------------------------------------------------------------
+
+def dgrad(seed: int = 0, T: int = 16384, Cout: int = 18432, Cin: int = 7168):
+    """Workload 6: the data gradient of the large FFN layer, dX [T, Cin] = dY W, with
+    dY [T, Cout] ~N(0, 1e-2) and the FFN weight W [Cout, Cin] ~N(0, 0.02) (the same stream
+    as workload 5's B when the sizes match)."""
+    dY = fill_bf16(NORMAL, key(6, 0, seed), (T, Cout), 1e-2)
+    W = fill_bf16(NORMAL, key(5, 2, seed), (Cout, Cin), 0.02)
+    return {"dY": dY, "W": W}
+
 
 def moe_tokens(seed: int = 0, T: int = 4096, D: int = 7168):
     return fill_bf16(NORMAL, key(3, 0, seed), (T, D), 1.0)

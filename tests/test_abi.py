@@ -52,6 +52,14 @@ def test_status_strings_and_argument_errors(libpath):
     assert L.fp8_quant_1x128(vp(16), 4, 128, 128, 2, vp(16), 128, vp(16), 4, None) == b.EINVAL
     assert L.fp8_quant_1x128(vp(18), 4, 128, 128, 0, vp(16), 128, vp(16), 4, None) == b.EALIGN
     assert L.fp8_quant_128x128(vp(16), 4, 100, 128, vp(16), 128, vp(16), 1, None) == b.EINVAL
+    # transposed block quantiser: N % 16, q without s, unaligned transposed pitch
+    assert L.fp8_quant_128x128_t(vp(16), 24, 128, 128, None, 0, None, 0, vp(16), 32, vp(16), 1,
+                                 None) == b.EINVAL
+    assert L.fp8_quant_128x128_t(vp(16), 32, 128, 128, vp(16), 128, None, 0, vp(16), 32, vp(16), 1,
+                                 None) == b.EINVAL
+    assert L.fp8_quant_128x128_t(vp(16), 32, 128, 128, None, 0, None, 0, vp(16), 40, vp(16), 1,
+                                 None) == b.EALIGN
+    assert L.fp8_quant_128x128_t(None, 0, 128, 128, None, 0, None, 0, None, 0, None, 0, None) == b.OK
     assert L.fp8_gemm_blockscaled(vp(16), 128, vp(16), 4, vp(16), 128, vp(16), 1, 0, vp(16), 8, 0,
                                   4, 8, 100, None) == b.EINVAL
     assert L.fp8_gemm_blockscaled(vp(16), 128, vp(16), 4, vp(16), 128, vp(16), 1, 2, vp(16), 8, 0,

@@ -73,6 +73,34 @@ def test_ffn_sampled_rows(fb, orc):
     _dense(fb, orc, d["A"], d["B"], rows=rows, what="ffn")
 
 
+def _dgrad(fb, orc, dY, W, rows=None, what=""):
+    """dX = dY W: dY quantised 1x128 along its channels, W through the transposed block quantiser."""
+    qdy, sdy = fb.quant_1x128(dev(dY))
+    _, _, qwt, swt = fb.quant_128x128_t(dev(W), straight=False)
+    C = fb.gemm_blockscaled(qdy, sdy, qwt, swt, 0, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert fb.get_device_error() == 0
+    oqdy, osdy = orc.quant_1x128_rows(dY)
+    _, _, oqwt, oswt = orc.quant_128x128_t(W)
+    if rows is None:
+        rows = np.arange(dY.shape[0])
+    ref = orc.bf16_round(orc.gemm_blockscaled(oqdy, osdy, oqwt, oswt, 0, rows=rows))
+    got = host_bits(C[torch.from_numpy(rows).cuda()])
+    return assert_gemm_close(got, ref, what)
+
+
+@pytest.mark.parametrize("T,Cout,Cin", [(200, 384, 384), (129, 256, 128), (1, 1536, 640)])
+def test_dgrad_small(fb, orc, tile_n, T, Cout, Cin):
+    d = synth.dgrad(T=T, Cout=Cout, Cin=Cin)
+    _dgrad(fb, orc, d["dY"], d["W"], what=f"dgrad {T}x{Cin}x{Cout}")
+
+
+def test_dgrad_full_size_sampled(fb, orc):
+    d = synth.dgrad()
+    rows = sample_rows(16384, 128, seed=7, must=(0, 127, 128, 16383))
+    _dgrad(fb, orc, d["dY"], d["W"], rows=rows, what="dgrad")
+
+
 def _wgrad(fb, orc, dY, X, rows=None, what=""):
     qdy, sdy = fb.quant_1x128(dev(dY), along=1)   # [Cout, T], [T/128, Cout]
     qx, sx = fb.quant_1x128(dev(X), along=1)      # [Cin, T],  [T/128, Cin]

@@ -2,7 +2,7 @@
 against the oracle (codes and scales), through the C ABI.
 
 Sizes: small ragged cases that span several tiles plus the full tensors of
-every workload (tiny, MLA, MoE sampled experts, Wgrad, FFN)."""
+every workload (tiny, MLA, MoE sampled experts, Wgrad, FFN, Dgrad weights)."""
 import numpy as np
 import pytest
 import torch
@@ -45,6 +45,27 @@ def _cols(fb, orc, x_bits):
     assert np.array_equal(s.cpu().numpy(), sr), "scales differ"
     bad = np.count_nonzero(q.cpu().numpy() != qr)
     assert bad == 0, f"{bad} codes differ"
+
+
+def _block_t(fb, orc, w_bits, straight=True):
+    q, s, qt, st = fb.quant_128x128_t(dev(w_bits), straight=straight)
+    torch.cuda.synchronize()
+    qr, sr, qtr, str_ = orc.quant_128x128_t(w_bits)
+    assert np.array_equal(st.cpu().numpy(), str_), "transposed scales differ"
+    bad = np.count_nonzero(qt.cpu().numpy() != qtr)
+    assert bad == 0, f"{bad} transposed codes differ"
+    if straight:
+        assert np.array_equal(s.cpu().numpy(), sr), "scales differ"
+        bad = np.count_nonzero(q.cpu().numpy() != qr)
+        assert bad == 0, f"{bad} codes differ"
+
+
+def _wide_range(rng, R, C):
+    """Tiles whose scales span ~2^-60 .. 2^60, with exact zeros, -0 and subnormal inputs."""
+    x = rng.standard_normal((R, C)).astype(np.float32)
+    x *= np.exp2(rng.integers(-60, 60, (R // 128 + 1, C // 128))).repeat(128, axis=0)[:R].repeat(
+        128, axis=1).astype(np.float32)
+    return x
 
 
 def test_fast_quotient_equals_ieee_divide_on_whole_bf16_domain(fb):
@@ -113,6 +134,53 @@ def test_mla_full(fb, orc):
 def test_cols_small_ragged(fb, orc):
     for (T, C, seed) in [(128, 8, 1), (384, 200, 2), (512, 1032, 3)]:
         _cols(fb, orc, synth.fill_bf16(synth.NORMAL, synth.key(93, seed), (T, C), 1e-2))
+
+
+def test_cols_wide_dynamic_range(fb, orc):
+    rng = np.random.default_rng(1)
+    x = _wide_range(rng, 384, 1024)
+    x[:128, 3] = 0.0
+    x[128:256, 130] = -0.0
+    x[256:, 260] = 1e-38
+    _cols(fb, orc, (x.view(np.uint32) >> 16).astype(np.uint16))
+
+
+def test_block_t_small_ragged(fb, orc):
+    for (N, K, seed) in [(16, 128, 1), (144, 256, 2), (576, 512, 3), (384, 1024, 4)]:
+        w = synth.fill_bf16(synth.OUTLIER, synth.key(98, seed), (N, K), 0.02, 0.01, 40.0, k2=synth.key(99, seed))
+        _block_t(fb, orc, w)
+        _block_t(fb, orc, w, straight=False)
+
+
+def test_block_t_wide_dynamic_range(fb, orc):
+    rng = np.random.default_rng(2)
+    x = _wide_range(rng, 400, 640)
+    x[:128, :128] = 0.0
+    x[128:256, 128:256] = -0.0
+    x[256:384, 256:384] = 1e-38
+    _block_t(fb, orc, (x.view(np.uint32) >> 16).astype(np.uint16))
+
+
+def test_block_t_strided(fb, orc):
+    """Leading dimensions larger than the used widths (16-byte multiples)."""
+    w = synth.fill_bf16(synth.NORMAL, synth.key(94, 1), (160, 400), 0.02)
+    x = dev(w)[:, :256]
+    qt = torch.zeros((256, 176), dtype=torch.uint8, device="cuda")[:, :160]
+    st = torch.zeros((2, 4), dtype=torch.float32, device="cuda")[:, :2]
+    q = torch.zeros((160, 272), dtype=torch.uint8, device="cuda")[:, :256]
+    s = torch.zeros((2, 4), dtype=torch.float32, device="cuda")[:, :2]
+    fb.quant_128x128_t(x, q=q, s=s, qt=qt, st=st)
+    torch.cuda.synchronize()
+    qr, sr, qtr, str_ = orc.quant_128x128_t(np.ascontiguousarray(w[:, :256]))
+    assert np.array_equal(qt.cpu().numpy(), qtr) and np.array_equal(st.cpu().numpy(), str_)
+    assert np.array_equal(q.cpu().numpy(), qr) and np.array_equal(s.cpu().numpy(), sr)
+
+
+def test_block_t_full_weights(fb, orc):
+    d = synth.mla()
+    _block_t(fb, orc, d["Wq"])
+    _block_t(fb, orc, d["Wkv"])  # 576 rows: last block is 64 rows
+    _block_t(fb, orc, synth.dgrad(T=128)["W"])  # 18432 x 7168
 
 
 def test_wgrad_full(fb, orc):

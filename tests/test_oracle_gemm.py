@@ -131,6 +131,31 @@ def test_lossless_inputs_give_exact_gemm(orc):
     assert np.all(np.abs(out - exact) <= tol)
 
 
+def test_dgrad_lossless_inputs_give_exact_product(orc):
+    """dX = dY W from dY's 1x128 codes and the transposed 128x128 weight codes: with
+    lossless inputs it is the exact double product (a transposed operand or scale grid
+    would not be)."""
+    rng = np.random.default_rng(10)
+    T, Cout, Cin = 16, 256, 384
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    cy = rng.choice(finite, (T, Cout))
+    cw = rng.choice(finite, (Cout, Cin))
+    cy[:, ::128] = 0x7E
+    cw[::128, ::128] = 0xFE
+    jy = rng.integers(-6, 6, (T, Cout // 128))
+    jw = rng.integers(-12, -4, (Cout // 128, Cin // 128))
+    vy = _dec_torch(cy) * np.exp2(np.repeat(jy, 128, axis=1))
+    vw = _dec_torch(cw) * np.exp2(np.repeat(np.repeat(jw, 128, axis=0), 128, axis=1))
+    yb = (vy.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    wb = (vw.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    qy, sy = orc.quant_1x128_rows(yb)
+    _, _, qwt, swt = orc.quant_128x128_t(wb)
+    out = orc.gemm_blockscaled(qy, sy, qwt, swt, 0).astype(np.float64)
+    exact = vy @ vw
+    tol = 4 * 2.0 ** -24 * (np.abs(vy) @ np.abs(vw))
+    assert np.all(np.abs(out - exact) <= tol)
+
+
 def test_row_subset_matches_full(orc):
     qa, sa, qb, sb, _ = _tiny_quantised(orc, M=20, N=200, K=256)
     full = orc.gemm_blockscaled(qa, sa, qb, sb, 0)

@@ -156,3 +156,18 @@ def test_block_matches_independent_restatement(orc):
             y = np.clip((blk / sc).astype(np.float32), -448, 448)
             ref = torch.from_numpy(np.ascontiguousarray(y)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
             assert np.array_equal(q[nb * 128:(nb + 1) * 128, kb * 128:(kb + 1) * 128], ref)
+
+
+def test_block_transpose_is_quantisation_of_transpose(orc):
+    """Quantising W^T directly gives the transposed codes and block scales (a 128x128 block
+    is the same set of elements either way); the partial last block row survives the swap."""
+    for N, K, seed in ((256, 384, 1), (384, 128, 2)):
+        w = synth.fill_bf16(synth.OUTLIER, synth.key(95, seed), (N, K), 0.02, 0.02, 40.0, k2=synth.key(96, seed))
+        q, s, qt, st = orc.quant_128x128_t(w)
+        q2, s2 = orc.quant_128x128(np.ascontiguousarray(w.T))
+        assert np.array_equal(qt, q2) and np.array_equal(st, s2)
+        assert np.array_equal(qt.T, q) and np.array_equal(st.T, s)
+    w = synth.fill_bf16(synth.NORMAL, synth.key(97, 0), (144, 256), 0.02)
+    q, s, qt, st = orc.quant_128x128_t(w)
+    assert qt.shape == (256, 144) and st.shape == (2, 2)
+    assert np.array_equal(qt[:, 128:], orc.quant_128x128(w[128:])[0].T)
