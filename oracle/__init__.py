@@ -9,7 +9,8 @@ the CUDA library.
 Sources: "DeepSeek-V3 技术报告：从 671B MoE 到低成本训练系统" (xutianle.me)
 §6 (FP8 GEMMs for Fprop/Dgrad/Wgrad, outputs in BF16 or FP32), §6.1 (1x128
 activation tiles, 128x128 weight blocks, online scales), §6.2 (FP32 promotion
-after every 128 FP8 products).
+after every 128 FP8 products), §2 and §4 (the MoE layer: sigmoid routing with
+a selection bias, top-8 of 256 experts, SwiGLU experts).
 
 Parity pins: every function here is pinned by ``tests/test_oracle_*.py``
 against the format definition, torch's independent float8_e4m3fn
@@ -69,6 +70,16 @@ def lib():
         L.orc_e4m3_encode_buffer.restype = None
         L.orc_e4m3_encode_patterns.argtypes = [ctypes.c_uint64, i64, vp, i32]
         L.orc_e4m3_encode_patterns.restype = None
+        L.orc_route_logits.argtypes = [vp, i64, i64, i64, vp, i64, i64, vp, i32]
+        L.orc_route_logits.restype = None
+        L.orc_route_select.argtypes = [vp, i64, i64, vp, i32, vp, vp]
+        L.orc_route_select.restype = None
+        L.orc_route_permute.argtypes = [vp, i64, i32, i64, vp, vp, vp]
+        L.orc_route_permute.restype = None
+        L.orc_swiglu_quant.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, i32]
+        L.orc_swiglu_quant.restype = None
+        L.orc_moe_combine.argtypes = [vp, i64, i64, vp, vp, i64, i32, vp, i64, i32]
+        L.orc_moe_combine.restype = None
         _lib = L
     return _lib
 
@@ -223,4 +234,71 @@ def grouped_gemm(A: np.ndarray, sa: np.ndarray, B: np.ndarray, sb: np.ndarray,
     for e in np.unique(expert_of):
         sel = np.nonzero(expert_of == e)[0]
         out[sel] = gemm_blockscaled(A, sa, B[e], sb[e], 0, rows[sel], threads)
+    return out
+
+
+# --- the MoE chain (V3 report §2 DeepSeekMoE, §4 aux-loss-free routing) ----
+
+def route_logits(x_bf16: np.ndarray, centroids: np.ndarray, threads: int | None = None) -> np.ndarray:
+    """Affinity logits l[t, e] = u_t . c_e in FP32, one fused multiply-add per term in k
+    order.  x_bf16: uint16 [T, D]; centroids: f32 [E, D].  Returns f32 [T, E]."""
+    x = _c(x_bf16, np.uint16)
+    c = _c(centroids, np.float32)
+    T, D = x.shape
+    E = c.shape[0]
+    out = np.empty((T, E), np.float32)
+    lib().orc_route_logits(_p(x), T, D, D, _p(c), D, E, _p(out), threads or nthreads())
+    return out
+
+
+def route_select(logits: np.ndarray, bias: np.ndarray, topk: int):
+    """Top-k experts per token by sigmoid(l) + b (double; ties to the lower index), listed in
+    increasing expert order, with gates s_e / sum of the chosen s.  Returns (sel int32 [T, k],
+    gate f32 [T, k])."""
+    l = _c(logits, np.float32)
+    b = _c(bias, np.float32)
+    T, E = l.shape
+    assert 0 < topk <= E
+    sel = np.empty((T, topk), np.int32)
+    gate = np.empty((T, topk), np.float32)
+    lib().orc_route_select(_p(l), T, E, _p(b), topk, _p(sel), _p(gate))
+    return sel, gate
+
+
+def route_permute(sel: np.ndarray, E: int):
+    """Rows grouped by expert, tokens in increasing order within an expert.  Returns
+    (offsets int32 [E+1], token_of_row int32 [T*k], row_of int32 [T, k])."""
+    sel = _c(sel, np.int32)
+    T, k = sel.shape
+    offsets = np.empty(E + 1, np.int32)
+    tor = np.empty(T * k, np.int32)
+    row_of = np.empty((T, k), np.int32)
+    lib().orc_route_permute(_p(sel), T, k, E, _p(offsets), _p(tor), _p(row_of))
+    return offsets, tor, row_of
+
+
+def swiglu_quant(acc: np.ndarray, threads: int | None = None):
+    """SwiGLU of up-projection accumulators acc f32 [R, 2*Nh] (gate | up) and its 1x128
+    quantisation.  Returns codes uint8 [R, Nh] and scales f32 [Nh/128, R]."""
+    a = _c(acc, np.float32)
+    R, N2 = a.shape
+    Nh = N2 // 2
+    assert N2 == 2 * Nh and Nh % 128 == 0
+    q = np.empty((R, Nh), np.uint8)
+    s = np.empty((Nh // 128, R), np.float32)
+    lib().orc_swiglu_quant(_p(a), R, Nh, N2, _p(q), Nh, _p(s), R, threads or nthreads())
+    return q, s
+
+
+def moe_combine(Y_bf16: np.ndarray, row_of: np.ndarray, gate: np.ndarray,
+                threads: int | None = None) -> np.ndarray:
+    """y[t] = sum_j gate[t, j] * Y[row_of[t, j]] (FP32 fused multiply-adds in j order, then
+    BF16).  Y_bf16: uint16 [R, N].  Returns uint16 [T, N]."""
+    Y = _c(Y_bf16, np.uint16)
+    row_of = _c(row_of, np.int32)
+    gate = _c(gate, np.float32)
+    T, k = row_of.shape
+    N = Y.shape[1]
+    out = np.empty((T, N), np.uint16)
+    lib().orc_moe_combine(_p(Y), N, N, _p(row_of), _p(gate), T, k, _p(out), N, threads or nthreads())
     return out

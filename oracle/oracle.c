@@ -417,3 +417,183 @@ void orc_e4m3_encode_patterns(uint64_t lo, int64_t n, uint8_t *q, int nthreads)
     encp_ctx c = {lo, q, n, 1 << 16};
     parallel_for((n + c.chunk - 1) / c.chunk, nthreads, encp_chunk, &c);
 }
+
+/* ======================================================================== */
+/* The MoE chain ([V3-report] §2 DeepSeekMoE: 256 routed experts, 8 per     */
+/* token, SwiGLU experts; §4 无辅助损失负载均衡: sigmoid affinity to each    */
+/* expert's centroid, selection by affinity + bias, gate from the affinity  */
+/* normalised over the selected experts).                                   */
+/* ======================================================================== */
+
+/* Affinity logits l[t][e] = u_t . c_e in FP32: one fused multiply-add per  */
+/* term, in k order.  The routing decision is taken in this precision and   */
+/* order on both sides (the kernel's), so the logits are reproducible bit   */
+/* for bit.  x: BF16 [T][ldx] (D used); c: FP32 [E][ldc]; l: FP32 [T][E].   */
+typedef struct {
+    const uint16_t *x;
+    int64_t D, ldx;
+    const float *c;
+    int64_t ldc, E;
+    float *l;
+} rl_ctx;
+
+static void rl_token(void *p, int64_t t)
+{
+    rl_ctx *c = (rl_ctx *)p;
+    const uint16_t *u = c->x + t * c->ldx;
+    for (int64_t e = 0; e < c->E; ++e) {
+        const float *ce = c->c + e * c->ldc;
+        float acc = 0.0f;
+        for (int64_t k = 0; k < c->D; ++k)
+            acc = fmaf(bf16_to_f32(u[k]), ce[k], acc);
+        c->l[t * c->E + e] = acc;
+    }
+}
+
+void orc_route_logits(const uint16_t *x, int64_t T, int64_t D, int64_t ldx,
+                      const float *c, int64_t ldc, int64_t E, float *l, int nthreads)
+{
+    rl_ctx ctx = {x, D, ldx, c, ldc, E, l};
+    parallel_for(T, nthreads, rl_token, &ctx);
+}
+
+/* Selection: affinity s_e = 1 / (1 + exp(-l_e)) and key_e = s_e + b_e in   */
+/* double; the top-k keys win, a tie going to the lower expert index.  The  */
+/* chosen experts are listed in increasing index order; their gates are     */
+/* fl32(s_e / sum of the chosen s), the sum taken in that order in double.  */
+void orc_route_select(const float *l, int64_t T, int64_t E, const float *bias, int topk,
+                      int32_t *sel, float *gate)
+{
+    double *key = (double *)malloc((size_t)E * sizeof(double));
+    double *s = (double *)malloc((size_t)E * sizeof(double));
+    char *taken = (char *)malloc((size_t)E);
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t e = 0; e < E; ++e) {
+            s[e] = 1.0 / (1.0 + exp(-(double)l[t * E + e]));
+            key[e] = s[e] + (double)bias[e];
+            taken[e] = 0;
+        }
+        for (int j = 0; j < topk; ++j) {
+            int64_t best = -1;
+            for (int64_t e = 0; e < E; ++e)
+                if (!taken[e] && (best < 0 || key[e] > key[best]))
+                    best = e;
+            if (best < 0)
+                break; /* topk > E: every expert is chosen */
+            taken[best] = 1;
+        }
+        int j = 0;
+        double sum = 0.0;
+        for (int64_t e = 0; e < E; ++e)
+            if (taken[e]) {
+                sel[t * topk + j++] = (int32_t)e;
+                sum += s[e];
+            }
+        for (j = 0; j < topk; ++j)
+            gate[t * topk + j] = (float)(s[sel[t * topk + j]] / sum);
+    }
+    free(key);
+    free(s);
+    free(taken);
+}
+
+/* Grouping: rows of expert e are offsets[e] .. offsets[e+1]-1, holding the */
+/* tokens that chose e in increasing token order.  token_of_row[r] is the   */
+/* token of row r; row_of[t*topk + j] is the row of token t's j-th expert.  */
+void orc_route_permute(const int32_t *sel, int64_t T, int topk, int64_t E,
+                       int32_t *offsets, int32_t *token_of_row, int32_t *row_of)
+{
+    offsets[0] = 0;
+    for (int64_t e = 0; e < E; ++e) {
+        int32_t n = 0;
+        for (int64_t i = 0; i < T * topk; ++i)
+            n += (sel[i] == e);
+        offsets[e + 1] = offsets[e] + n;
+    }
+    for (int64_t e = 0; e < E; ++e) {
+        int32_t r = offsets[e];
+        for (int64_t t = 0; t < T; ++t)
+            for (int j = 0; j < topk; ++j)
+                if (sel[t * topk + j] == e) {
+                    token_of_row[r] = (int32_t)t;
+                    row_of[t * topk + j] = r;
+                    ++r;
+                }
+    }
+}
+
+/* SwiGLU of one expert's up-projection and its 1x128 quantisation: from    */
+/* the FP32 accumulators gate g = acc[r][i] and up u = acc[r][Nh + i],      */
+/* h = g / (1 + exp(-g)) * u in double, rounded once to FP32; then the      */
+/* 1x128 tiles of h as for activations: amax over |h| (FP32), scale =       */
+/* amax / 448 (IEEE single), codes = E4M3(fl32(h / scale)).                 */
+/* acc: FP32 [R][ldacc] (2*Nh used); q: [R][ldq]; s: FP32 [Nh/128][lds].    */
+typedef struct {
+    const float *acc;
+    int64_t Nh, ldacc;
+    uint8_t *q;
+    int64_t ldq;
+    float *s;
+    int64_t lds;
+} sw_ctx;
+
+static void sw_row(void *p, int64_t r)
+{
+    sw_ctx *c = (sw_ctx *)p;
+    const float *a = c->acc + r * c->ldacc;
+    float h[128];
+    for (int64_t kb = 0; kb < c->Nh / 128; ++kb) {
+        float amax = 0.0f;
+        for (int i = 0; i < 128; ++i) {
+            double g = a[kb * 128 + i], u = a[c->Nh + kb * 128 + i];
+            h[i] = (float)(g / (1.0 + exp(-g)) * u);
+            float m = fabsf(h[i]);
+            if (m > amax)
+                amax = m;
+        }
+        float sc = orc_tile_scale(amax);
+        c->s[kb * c->lds + r] = sc;
+        for (int i = 0; i < 128; ++i)
+            c->q[r * c->ldq + kb * 128 + i] = orc_e4m3_encode(h[i] / sc);
+    }
+}
+
+void orc_swiglu_quant(const float *acc, int64_t R, int64_t Nh, int64_t ldacc,
+                      uint8_t *q, int64_t ldq, float *s, int64_t lds, int nthreads)
+{
+    sw_ctx c = {acc, Nh, ldacc, q, ldq, s, lds};
+    parallel_for(R, nthreads, sw_row, &c);
+}
+
+/* Combine: y[t][n] = sum_j gate[t][j] * Y[row_of[t][j]][n], one FP32 fused */
+/* multiply-add per expert in the listed (increasing expert) order, from    */
+/* the BF16 expert outputs; the result rounded to BF16 (RNE).               */
+typedef struct {
+    const uint16_t *Y;
+    int64_t ldy, N;
+    const int32_t *row_of;
+    const float *gate;
+    int topk;
+    uint16_t *out;
+    int64_t ldo;
+} cb_ctx;
+
+static void cb_token(void *p, int64_t t)
+{
+    cb_ctx *c = (cb_ctx *)p;
+    for (int64_t n = 0; n < c->N; ++n) {
+        float acc = 0.0f;
+        for (int j = 0; j < c->topk; ++j)
+            acc = fmaf(c->gate[t * c->topk + j],
+                       bf16_to_f32(c->Y[(int64_t)c->row_of[t * c->topk + j] * c->ldy + n]), acc);
+        c->out[t * c->ldo + n] = orc_bf16_rne(acc);
+    }
+}
+
+void orc_moe_combine(const uint16_t *Y, int64_t ldy, int64_t N, const int32_t *row_of,
+                     const float *gate, int64_t T, int topk, uint16_t *out, int64_t ldo,
+                     int nthreads)
+{
+    cb_ctx c = {Y, ldy, N, row_of, gate, topk, out, ldo};
+    parallel_for(T, nthreads, cb_token, &c);
+}

@@ -179,6 +179,14 @@ def moe_route(tokens_bf16: np.ndarray, E: int = 256, topk: int = 8, seed: int = 
     return offsets.astype(np.int32), tokens[perm]
 
 
+def moe_router(seed: int = 0, E: int = 256, D: int = 7168):
+    """Router inputs of workload 3: expert centroids f32 [E, D] ~N(0, 1/D) and selection
+    biases f32 [E] ~N(0, 0.5) (the streams moe_route draws from)."""
+    cent = fill_f32(NORMAL, key(3, 1, seed), (E, D), 1.0 / np.sqrt(D))
+    bias = fill_f32(NORMAL, key(3, 2, seed), (E,), 0.5)
+    return cent, bias
+
+
 def moe_weights(which: str, e_lo: int, e_hi: int, seed: int = 0,
                 N: int | None = None, K: int | None = None) -> np.ndarray:
     """Expert weights e_lo..e_hi-1 of the up (N=4096, K=7168) or down
