@@ -11,8 +11,12 @@ from .binding import (  # noqa: F401
     gemm_blockscaled,
     get_device_error,
     grouped_gemm_moe,
+    grouped_gemm_moe_swiglu,
     lib,
+    moe_combine,
+    moe_route,
     quant_1x128,
+    quant_1x128_gather,
     quant_128x128,
     quant_128x128_t,
     selftest_division,

@@ -20,7 +20,9 @@ OK, EINVAL, EALIGN, EARCH, ECUDA, ETIMEOUT = 0, -1, -2, -3, -4, -5
 # every symbol include/fp8bs.h declares
 EXPORTS = (
     "fp8_quant_1x128", "fp8_quant_128x128", "fp8_quant_128x128_t", "fp8_gemm_blockscaled",
-    "fp8_grouped_gemm_moe", "fp8bs_e4m3_encode", "fp8bs_status_string", "fp8bs_get_device_error",
+    "fp8_grouped_gemm_moe", "fp8_moe_route_workspace_size", "fp8_moe_route", "fp8_quant_1x128_gather",
+    "fp8_grouped_gemm_moe_swiglu", "fp8_moe_combine", "fp8bs_e4m3_encode", "fp8bs_status_string",
+    "fp8bs_get_device_error",
     "fp8bs_selftest_timeout", "fp8bs_selftest_division", "fp8bs_set_gemm_tile_n", "fp8bs_version",
 )
 
@@ -47,6 +49,13 @@ def lib() -> ctypes.CDLL:
         L.fp8_quant_128x128_t.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp]
         L.fp8_gemm_blockscaled.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i32, vp, i64, i32, i64, i64, i64, vp]
         L.fp8_grouped_gemm_moe.argtypes = [vp, i64, vp, i64, vp, vp, vp, i32, i64, vp, i64, i32, i64, i64, vp]
+        L.fp8_moe_route_workspace_size.argtypes = [i32]
+        L.fp8_moe_route_workspace_size.restype = i64
+        L.fp8_moe_route.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, i64, vp]
+        L.fp8_quant_1x128_gather.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp]
+        L.fp8_grouped_gemm_moe_swiglu.argtypes = [vp, i64, vp, i64, vp, vp, vp, i32, i64, vp, i64, vp, i64, i64,
+                                                  i64, vp]
+        L.fp8_moe_combine.argtypes = [vp, i64, i64, vp, vp, i64, i32, i64, vp, i64, vp]
         L.fp8bs_e4m3_encode.argtypes = [vp, vp, i64, vp]
         L.fp8bs_status_string.argtypes = [i32]
         L.fp8bs_status_string.restype = ctypes.c_char_p
@@ -56,7 +65,8 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_set_gemm_tile_n.argtypes = [i32]
         L.fp8bs_version.restype = ctypes.c_char_p
         for name in ("fp8_quant_1x128", "fp8_quant_128x128", "fp8_quant_128x128_t", "fp8_gemm_blockscaled",
-                     "fp8_grouped_gemm_moe", "fp8bs_e4m3_encode", "fp8bs_get_device_error",
+                     "fp8_grouped_gemm_moe", "fp8_moe_route", "fp8_quant_1x128_gather",
+                     "fp8_grouped_gemm_moe_swiglu", "fp8_moe_combine", "fp8bs_e4m3_encode", "fp8bs_get_device_error",
                      "fp8bs_selftest_timeout", "fp8bs_selftest_division", "fp8bs_set_gemm_tile_n"):
             getattr(L, name).restype = i32
         _lib = L
@@ -168,6 +178,67 @@ def set_gemm_tile_n(bn: int) -> None:
 
 def get_device_error(stream=None) -> int:
     return lib().fp8bs_get_device_error(_stream(stream))
+
+
+def moe_route(x: torch.Tensor, centroids: torch.Tensor, bias: torch.Tensor, topk: int, out=None,
+              workspace=None, stream=None):
+    """Routing of BF16 tokens x [T, D] over E experts (centroids f32 [E, D], bias f32 [E]).
+    Returns a dict of device tensors: logits [T, E], expert_idx [T, k], gate [T, k],
+    offsets [E+1], token_of_row [T*k], row_of [T, k] (int32 / f32)."""
+    T, D = x.shape
+    E = centroids.shape[0]
+    dev = x.device
+    o = out if out is not None else {
+        "logits": torch.empty((T, E), dtype=torch.float32, device=dev),
+        "expert_idx": torch.empty((T, topk), dtype=torch.int32, device=dev),
+        "gate": torch.empty((T, topk), dtype=torch.float32, device=dev),
+        "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+        "token_of_row": torch.empty(T * topk, dtype=torch.int32, device=dev),
+        "row_of": torch.empty((T, topk), dtype=torch.int32, device=dev),
+    }
+    nbytes = lib().fp8_moe_route_workspace_size(E)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    _check("fp8_moe_route", lib().fp8_moe_route(
+        _ptr(x), T, D, _ld(x), _ptr(centroids), _ld(centroids), _ptr(bias), E, topk,
+        _ptr(o["logits"]), _ptr(o["expert_idx"]), _ptr(o["gate"]), _ptr(o["offsets"]),
+        _ptr(o["token_of_row"]), _ptr(o["row_of"]), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return o
+
+
+def quant_1x128_gather(x: torch.Tensor, row_map: torch.Tensor, q=None, s=None, stream=None):
+    """1x128 quantisation of the rows x[row_map[r]]: q [R, K], s [K/128, R]."""
+    T, K = x.shape
+    R = row_map.numel()
+    q = torch.empty((R, K), dtype=torch.uint8, device=x.device) if q is None else q
+    s = torch.empty((K // 128, R), dtype=torch.float32, device=x.device) if s is None else s
+    _check("fp8_quant_1x128_gather", lib().fp8_quant_1x128_gather(
+        _ptr(x), T, K, _ld(x), _ptr(row_map), R, _ptr(q), _ld(q), _ptr(s), _ld(s), _stream(stream)))
+    return q, s
+
+
+def grouped_gemm_moe_swiglu(A, sa, B, sb, offsets, Q=None, s=None, stream=None):
+    """Up projection [G, 2*Nh, K] (gate rows, then up rows) with SwiGLU + 1x128 quantisation
+    fused: returns codes Q [M_total, Nh] and scales s [Nh/128, M_total]."""
+    M, K = A.shape
+    G, N2, _ = B.shape
+    Nh = N2 // 2
+    Q = torch.empty((M, Nh), dtype=torch.uint8, device=A.device) if Q is None else Q
+    s = torch.empty((Nh // 128, M), dtype=torch.float32, device=A.device) if s is None else s
+    _check("fp8_grouped_gemm_moe_swiglu", lib().fp8_grouped_gemm_moe_swiglu(
+        _ptr(A), _ld(A), _ptr(sa), _ld(sa), _ptr(B), _ptr(sb), _ptr(offsets), G, M, _ptr(Q), _ld(Q),
+        _ptr(s), _ld(s), Nh, K, _stream(stream)))
+    return Q, s
+
+
+def moe_combine(Y: torch.Tensor, row_of: torch.Tensor, gate: torch.Tensor, out=None, stream=None):
+    """out[t] = sum_j gate[t, j] * Y[row_of[t, j]] (BF16)."""
+    R, N = Y.shape
+    T, k = row_of.shape
+    out = torch.empty((T, N), dtype=torch.bfloat16, device=Y.device) if out is None else out
+    _check("fp8_moe_combine", lib().fp8_moe_combine(
+        _ptr(Y), _ld(Y), R, _ptr(row_of), _ptr(gate), T, k, N, _ptr(out), _ld(out), _stream(stream)))
+    return out
 
 
 def selftest_division(stream=None):

@@ -11,6 +11,7 @@
 
 #include "../../include/fp8bs.h"
 #include "gemm.cuh"
+#include "moe.cuh"
 #include "ptx.cuh"
 #include "quant.cuh"
 
@@ -121,13 +122,15 @@ int make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t 
 }
 
 // ------------------------------------------------------------------ GEMM
-template <int BN, int BMODE, bool OUT_F32, bool GROUPED>
+template <int BN, int BMODE, bool OUT_F32, bool GROUPED, bool SWIGLU = false>
 int launch_gemm(DeviceInfo *d, const CUtensorMap &tA, const CUtensorMap &tB, const CUtensorMap &tSB,
                 const gemm::Params &p, int grid, cudaStream_t st)
 {
     using C = gemm::Cfg<BN, BMODE, GROUPED>;
-    auto kern = gemm::gemm_kernel<BN, BMODE, OUT_F32, GROUPED>;
-    constexpr int inst_bit = (BN == 256 ? 0 : BN == 192 ? 1 : 2) * 8 + BMODE * 4 + (OUT_F32 ? 2 : 0) + (GROUPED ? 1 : 0);
+    auto kern = gemm::gemm_kernel<BN, BMODE, OUT_F32, GROUPED, SWIGLU>;
+    constexpr int inst_bit = SWIGLU ? 24 + (GROUPED ? 1 : 0)
+                                    : (BN == 256 ? 0 : BN == 192 ? 1 : 2) * 8 + BMODE * 4 + (OUT_F32 ? 2 : 0) +
+                                          (GROUPED ? 1 : 0);
     {
         std::lock_guard<std::mutex> lk(g_mu);
         if (!(d->gemm_attr_set & (1u << inst_bit))) {
@@ -148,9 +151,6 @@ int launch_gemm_bn(int bn, int out_dtype, DeviceInfo *d, const CUtensorMap &tA, 
         return out_dtype == 0 ? launch_gemm<256, BMODE, false, GROUPED>(d, tA, tB, tSB, p, grid, st)
                               : launch_gemm<256, BMODE, true, GROUPED>(d, tA, tB, tSB, p, grid, st);
     if constexpr (BMODE == 0) {
-        if (bn == 256)
-            return out_dtype == 0 ? launch_gemm<256, BMODE, false, GROUPED>(d, tA, tB, tSB, p, grid, st)
-                                  : launch_gemm<256, BMODE, true, GROUPED>(d, tA, tB, tSB, p, grid, st);
         if (bn == 192)
             return out_dtype == 0 ? launch_gemm<192, BMODE, false, GROUPED>(d, tA, tB, tSB, p, grid, st)
                                   : launch_gemm<192, BMODE, true, GROUPED>(d, tA, tB, tSB, p, grid, st);
@@ -347,6 +347,8 @@ int fp8_gemm_blockscaled(const uint8_t *A, int64_t lda, const float *sa, int64_t
     p.sb_estride = 0;
     p.C = C;
     p.ldc = ldc;
+    p.s_out = nullptr;
+    p.lds_out = 0;
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
@@ -354,6 +356,8 @@ int fp8_gemm_blockscaled(const uint8_t *A, int64_t lda, const float *sa, int64_t
     p.G = 0;
 
     const int BN = pick_bn(M, N, b_scale_mode, d->num_sms);
+    p.tile_n = BN;
+    p.b_rows = static_cast<int>(N);
     CUtensorMap tA, tB, tSB;
     std::memset(&tSB, 0, sizeof tSB);
     if (make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, lda, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -398,6 +402,8 @@ int fp8_grouped_gemm_moe(const uint8_t *A, int64_t lda, const float *sa, int64_t
     p.sb_estride = ((N + 127) / 128) * (K / 128);
     p.C = C;
     p.ldc = ldc;
+    p.s_out = nullptr;
+    p.lds_out = 0;
     p.M = static_cast<int>(M_total);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
@@ -405,6 +411,8 @@ int fp8_grouped_gemm_moe(const uint8_t *A, int64_t lda, const float *sa, int64_t
     p.G = G;
 
     const int BN = pick_bn(M_total, N, 0, d->num_sms);
+    p.tile_n = BN;
+    p.b_rows = static_cast<int>(N);
     CUtensorMap tA, tB, tSB;
     std::memset(&tSB, 0, sizeof tSB);
     if (make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M_total, lda, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -414,6 +422,152 @@ int fp8_grouped_gemm_moe(const uint8_t *A, int64_t lda, const float *sa, int64_t
     const int64_t max_tiles = ((M_total + 127) / 128 + G) * ((N + BN - 1) / BN);
     const int grid = static_cast<int>(std::min<int64_t>(max_tiles, d->num_sms));
     return launch_gemm_bn<0, true>(BN, out_dtype, d, tA, tB, tSB, p, grid, static_cast<cudaStream_t>(stream));
+}
+
+int fp8_grouped_gemm_moe_swiglu(const uint8_t *A, int64_t lda, const float *sa, int64_t ldsa, const uint8_t *B,
+                                const float *sb, const int32_t *group_offsets, int G, int64_t M_total, uint8_t *Q,
+                                int64_t ldq, float *s, int64_t lds, int64_t Nh, int64_t K, void *stream)
+{
+    if (G < 1 || G > gemm::kMaxGroups || !group_offsets || M_total < 0 || Nh < 0 || K < 0)
+        return FP8BS_EINVAL;
+    if (M_total == 0 || Nh == 0)
+        return FP8BS_OK;
+    if (K == 0 || K % 128 != 0 || Nh % 128 != 0 || !A || !sa || !B || !sb || !Q || !s)
+        return FP8BS_EINVAL;
+    if (M_total >= (int64_t(1) << 31) || K >= (int64_t(1) << 31) || int64_t(G) * 2 * Nh >= (int64_t(1) << 31))
+        return FP8BS_EINVAL;
+    if (lda < K || ldsa < M_total || ldq < Nh || lds < M_total)
+        return FP8BS_EINVAL;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(Q) || lda % 16 != 0 || ldq % 16 != 0 ||
+        (reinterpret_cast<uintptr_t>(sa) & 3) || (reinterpret_cast<uintptr_t>(sb) & 3) ||
+        (reinterpret_cast<uintptr_t>(s) & 3) || (reinterpret_cast<uintptr_t>(group_offsets) & 3))
+        return FP8BS_EALIGN;
+    DeviceInfo *d;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK)
+        return rc;
+
+    gemm::Params p;
+    p.sa = sa;
+    p.ldsa = ldsa;
+    p.sb = sb;
+    p.ldsb = K / 128;
+    p.sb_estride = (2 * Nh / 128) * (K / 128);
+    p.C = Q;
+    p.ldc = ldq;
+    p.s_out = s;
+    p.lds_out = lds;
+    p.M = static_cast<int>(M_total);
+    p.N = static_cast<int>(Nh);
+    p.K = static_cast<int>(K);
+    p.tile_n = 128;
+    p.b_rows = static_cast<int>(2 * Nh);
+    p.offs = group_offsets;
+    p.G = G;
+
+    CUtensorMap tA, tB, tSB;
+    std::memset(&tSB, 0, sizeof tSB);
+    if (make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M_total, lda, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        make_map(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, int64_t(G) * 2 * Nh, K, 128, 128,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+        return FP8BS_EINVAL;
+    const int64_t max_tiles = ((M_total + 127) / 128 + G) * (Nh / 128);
+    const int grid = static_cast<int>(std::min<int64_t>(max_tiles, d->num_sms));
+    return launch_gemm<256, 0, false, true, true>(d, tA, tB, tSB, p, grid, static_cast<cudaStream_t>(stream));
+}
+
+int fp8_quant_1x128_gather(const void *x, int64_t T, int64_t K, int64_t ldx, const int32_t *row_map, int64_t R,
+                           uint8_t *q, int64_t ldq, float *s, int64_t lds, void *stream)
+{
+    if (T < 0 || K < 0 || R < 0)
+        return FP8BS_EINVAL;
+    if (R == 0 || K == 0)
+        return FP8BS_OK;
+    if (!x || !row_map || !q || !s || ldx < K || K % 128 != 0 || ldq < K || lds < R)
+        return FP8BS_EINVAL;
+    if (T > (int64_t(1) << 31) || R > (int64_t(1) << 31) || K > (int64_t(1) << 31))
+        return FP8BS_EINVAL;
+    if (!aligned16(x) || !aligned16(q) || (ldx * 2) % 16 != 0 || ldq % 16 != 0 ||
+        (reinterpret_cast<uintptr_t>(row_map) & 3))
+        return FP8BS_EALIGN;
+    DeviceInfo *d;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK)
+        return rc;
+    const int64_t tiles = ((R + 127) / 128) * (K / 128);
+    const int64_t grid = std::min<int64_t>(tiles, int64_t(d->num_sms) * d->quant_rows_ctas);
+    quant::quant_rows_kernel<false><<<static_cast<int>(grid), quant::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(x), R, K, ldx, q, ldq, s, lds, row_map, T);
+    return launch_status();
+}
+
+int64_t fp8_moe_route_workspace_size(int E)
+{
+    if (E < 1 || E > moe::kMaxExperts)
+        return -1;
+    return (static_cast<int64_t>(E) * 4 + 255) / 256 * 256;
+}
+
+int fp8_moe_route(const void *x, int64_t T, int64_t D, int64_t ldx, const float *centroids, int64_t ldc,
+                  const float *bias, int E, int topk, float *logits, int32_t *expert_idx, float *gate,
+                  int32_t *offsets, int32_t *token_of_row, int32_t *row_of, void *workspace,
+                  int64_t workspace_bytes, void *stream)
+{
+    if (T < 0 || D <= 0 || E < 1 || E > moe::kMaxExperts || topk < 1 || topk > moe::kMaxTopk || topk > E)
+        return FP8BS_EINVAL;
+    if (D % 32 != 0 || ldx < D || ldc < D || !offsets || !workspace ||
+        workspace_bytes < fp8_moe_route_workspace_size(E))
+        return FP8BS_EINVAL;
+    if (T > 0 && (!x || !centroids || !bias || !logits || !expert_idx || !gate || !token_of_row || !row_of))
+        return FP8BS_EINVAL;
+    if (T * topk >= (int64_t(1) << 31))
+        return FP8BS_EINVAL;
+    if ((T > 0 && (!aligned16(x) || !aligned16(centroids) || (ldx * 2) % 16 != 0 || (ldc * 4) % 16 != 0)) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return FP8BS_EALIGN;
+    DeviceInfo *d;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int *counts = static_cast<int *>(workspace);
+    if (T == 0) {
+        if (cudaMemsetAsync(counts, 0, static_cast<size_t>(E) * 4, st) != cudaSuccess)
+            return FP8BS_ECUDA;
+    } else {
+        const dim3 lg(static_cast<unsigned>((T + moe::kLT - 1) / moe::kLT), (E + moe::kLE - 1) / moe::kLE);
+        moe::route_logits_kernel<<<lg, 256, 0, st>>>(static_cast<const uint16_t *>(x), T, D, ldx, centroids, ldc, E,
+                                                     logits, counts);
+        const unsigned sg = static_cast<unsigned>((T + 7) / 8);
+        if (E <= 256)
+            moe::route_select_kernel<8><<<sg, 256, 0, st>>>(logits, T, E, bias, topk, expert_idx, gate, counts);
+        else
+            moe::route_select_kernel<32><<<sg, 256, 0, st>>>(logits, T, E, bias, topk, expert_idx, gate, counts);
+    }
+    moe::route_group_kernel<<<E, 256, 0, st>>>(expert_idx, T, topk, E, counts, offsets, token_of_row, row_of);
+    return launch_status();
+}
+
+int fp8_moe_combine(const void *Y, int64_t ldy, int64_t R, const int32_t *row_of, const float *gate, int64_t T,
+                    int topk, int64_t N, void *out, int64_t ldo, void *stream)
+{
+    if (T < 0 || N < 0 || R < 0 || topk < 1 || topk > moe::kMaxTopk)
+        return FP8BS_EINVAL;
+    if (T == 0 || N == 0)
+        return FP8BS_OK;
+    if (!Y || !row_of || !gate || !out || N % 8 != 0 || ldy < N || ldo < N)
+        return FP8BS_EINVAL;
+    if (!aligned16(Y) || !aligned16(out) || (ldy * 2) % 16 != 0 || (ldo * 2) % 16 != 0)
+        return FP8BS_EALIGN;
+    DeviceInfo *d;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK)
+        return rc;
+    const int64_t work = T * (N / 8);
+    const int64_t grid = std::min<int64_t>((work + 255) / 256, int64_t(d->num_sms) * 8);
+    moe::combine_kernel<<<static_cast<int>(grid), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(Y), ldy, R, row_of, gate, T, topk, N, static_cast<uint16_t *>(out), ldo);
+    return launch_status();
 }
 
 int fp8bs_e4m3_encode(const float *x, uint8_t *q, int64_t n, void *stream)

@@ -36,6 +36,15 @@
 //   tfull[b]  partial in TMEM buffer b is complete (tcgen05.commit -> promotion)
 //   tempty[b] promotion has read buffer b          (one arrival per promotion warp -> MMA)
 //   sbfull/sbempty  per-stage B row scales (row-scale mode only)
+//
+// SwiGLU variant (V3 report §2: SwiGLU experts; §6.1: the down projection
+// takes the 1x128-quantised SwiGLU output): B holds the gate rows [0, N) and
+// the up rows [N, 2N) of the up projection.  A 128 x 256 MMA tile loads gate
+// block j and up block j (two 128-row TMA boxes) and yields the 128 channels
+// 128j .. 128j+127: each promotion thread owns the gate and the up columns
+// of the same 64 channels, forms h = silu(g) * u from its FP32 accumulators,
+// the two warpgroups exchange their row amax, and the epilogue writes the
+// E4M3 codes and 1x128 scales of h instead of C.
 #pragma once
 #include <cstdint>
 
@@ -75,7 +84,8 @@ struct Cfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SBROW_BYTES;
     static constexpr int EPI_BYTES = NPW * 2048;
     static constexpr int TABLE_BYTES = GROUPED_ ? (kMaxGroups + 1) * 4 : 0;
-    static constexpr int FIXED = EPI_BYTES + TABLE_BYTES + 512 + 1024;  // + barriers, + alignment slack
+    static constexpr int XCH_BYTES = 2048;  // SwiGLU row-amax exchange, two tiles deep
+    static constexpr int FIXED = EPI_BYTES + XCH_BYTES + TABLE_BYTES + 512 + 1024;  // + barriers, + alignment slack
     // Even, so that every use of a stage falls to the same MMA issuer (chunks
     // c and c + STAGES have the same parity): each issuer then waits the
     // phases of its stages in order and can never mistake a stage's previous
@@ -87,8 +97,9 @@ struct Cfg {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SBROW = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_EPI = OFF_SBROW + STAGES * SBROW_BYTES;
-    static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
-    static constexpr int NBAR = 4 * STAGES + 2 * NTMEM;
+    static constexpr int OFF_XCH = OFF_EPI + EPI_BYTES;
+    static constexpr int OFF_BAR = OFF_XCH + XCH_BYTES;
+    static constexpr int NBAR = 4 * STAGES + 2 * NTMEM + 1;  // + the SwiGLU exchange barrier
     static constexpr int OFF_TMEMSLOT = OFF_BAR + NBAR * 8;
     static constexpr int OFF_TILESTART = (OFF_TMEMSLOT + 4 + 15) / 16 * 16;
     static constexpr int BYTES = OFF_TILESTART + TABLE_BYTES;
@@ -104,9 +115,13 @@ struct Params {
     const float *sb;     // BMODE 0: sb[nb*ldsb + kb] (per expert: + e*sb_estride)
     int64_t ldsb;
     int64_t sb_estride;
-    void *C;
+    void *C;             // output; SwiGLU: E4M3 codes of h
     int64_t ldc;
-    int M, N, K;         // M = rows of A (M_total when grouped)
+    float *s_out;        // SwiGLU: 1x128 scales of h, [N/128][lds_out]
+    int64_t lds_out;
+    int M, N, K;         // M = rows of A (M_total when grouped); N = output columns
+    int tile_n;          // output columns per tile (BN; SwiGLU: 128)
+    int b_rows;          // rows of B per expert (N; SwiGLU: 2N)
     const int32_t *offs; // grouped: [G+1] row offsets (device)
     int G;
 };
@@ -121,7 +136,7 @@ template <int BN, bool GROUPED>
 __device__ __forceinline__ Tile tile_of(int t, const Params &p, const int *tile_start)
 {
     Tile r;
-    const int num_n = (p.N + BN - 1) / BN;
+    const int num_n = (p.N + p.tile_n - 1) / p.tile_n;
     if constexpr (!GROUPED) {
         const int num_m = (p.M + BM - 1) / BM;
         const int per_group = kGroupM * num_n;
@@ -133,7 +148,7 @@ __device__ __forceinline__ Tile tile_of(int t, const Params &p, const int *tile_
         const int nt = local / gsize;
         r.m0 = mt * BM;
         r.m_end = p.M;
-        r.n0 = nt * BN;
+        r.n0 = nt * p.tile_n;
         r.brow0 = r.n0;
         r.sbp = p.sb;
         r.valid = true;
@@ -155,8 +170,8 @@ __device__ __forceinline__ Tile tile_of(int t, const Params &p, const int *tile_
         const int mt = local - nt * mtiles;
         r.m0 = base + mt * BM;
         r.m_end = base + m_e;
-        r.n0 = nt * BN;
-        r.brow0 = e * p.N + r.n0;
+        r.n0 = nt * p.tile_n;
+        r.brow0 = e * p.b_rows + r.n0;
         r.sbp = p.sb + static_cast<int64_t>(e) * p.sb_estride;
         r.valid = true;
     }
@@ -165,10 +180,10 @@ __device__ __forceinline__ Tile tile_of(int t, const Params &p, const int *tile_
 
 // Prefix sum of per-expert tile counts, computed by the promotion warps.
 // Malformed ranges (negative length or past M) count as empty.
-template <int BN, int NPW>
+template <int NPW>
 __device__ void build_tile_start(const Params &p, int *tile_start, int ptid)
 {
-    const int num_n = (p.N + BN - 1) / BN;
+    const int num_n = (p.N + p.tile_n - 1) / p.tile_n;
     __shared__ int warp_sums[NPW];
     // each promotion thread owns up to PER consecutive experts
     constexpr int PER = (kMaxGroups + NPW * 32 - 1) / (NPW * 32);
@@ -271,12 +286,13 @@ __device__ __forceinline__ void tmem_ld_wait_regs2(uint32_t (&r)[32], uint32_t (
                  : "memory");
 }
 
-template <int BN, int BMODE, bool OUT_F32, bool GROUPED>
+template <int BN, int BMODE, bool OUT_F32, bool GROUPED, bool SWIGLU = false>
 __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmSB, const Params p)
 {
     using L = Cfg<BN, BMODE, GROUPED>;
+    static_assert(!SWIGLU || (BN == 256 && BMODE == 0 && !OUT_F32), "SwiGLU: 128 x 256 tiles, block scales");
     constexpr int STAGES = L::STAGES;
     constexpr int NTMEM = L::NTMEM;
     extern __shared__ uint8_t dyn_smem_raw[];
@@ -292,6 +308,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
     const uint32_t bar_sbempty = bar_sbfull + 8 * STAGES;
     const uint32_t bar_tfull = bar_sbempty + 8 * STAGES;
     const uint32_t bar_tempty = bar_tfull + 8 * NTMEM;
+    const uint32_t bar_xch = bar_tempty + 8 * NTMEM;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_TMEMSLOT);
     int *tile_start = reinterpret_cast<int *>(smem + L::OFF_TILESTART);
 
@@ -306,6 +323,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
             mbar_init(bar_tfull + 8 * b, 1);
             mbar_init(bar_tempty + 8 * b, L::NPW);
         }
+        mbar_init(bar_xch, L::NPW * 32);
         fence_barrier_init();
         fence_proxy_async_smem();
     }
@@ -321,7 +339,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
     }
     if constexpr (GROUPED) {
         if (warp >= kFirstPromoWarp)
-            build_tile_start<BN, L::NPW>(p, tile_start, threadIdx.x - kFirstPromoWarp * 32);
+            build_tile_start<L::NPW>(p, tile_start, threadIdx.x - kFirstPromoWarp * 32);
     }
     tc_fence_before();
     __syncthreads();
@@ -352,7 +370,13 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                     }
                     mbar_arrive_expect_tx(bar_full + 8 * s, L::A_BYTES + L::B_BYTES);
                     tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmA, kb * BK, tl.m0, bar_full + 8 * s);
-                    tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, kb * BK, tl.brow0, bar_full + 8 * s);
+                    if constexpr (SWIGLU) {  // gate block, then up block (128-row boxes)
+                        tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, kb * BK, tl.brow0, bar_full + 8 * s);
+                        tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES + 128 * BK, &tmB, kb * BK, tl.brow0 + p.N,
+                                    bar_full + 8 * s);
+                    } else {
+                        tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, kb * BK, tl.brow0, bar_full + 8 * s);
+                    }
                     if constexpr (BMODE == 1) {
                         if (!mbar_wait(bar_sbempty + 8 * s, ph ^ 1, ERR_TIMEOUT_PRODUCER)) {
                             ok = false;
@@ -426,6 +450,8 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
         const float *sbrow_smem = reinterpret_cast<const float *>(smem + L::OFF_SBROW);
 
         uint32_t c = 0;
+        uint32_t tcount = 0;  // tiles finished (SwiGLU exchange phase)
+        (void)tcount;
         bool ok = true;
         for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
             const Tile tl = tile_of<BN, GROUPED>(t, p, tile_start);
@@ -435,7 +461,10 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
             // 128-column scale block
             int nb = (tl.n0 + col0) / 128;
             nb = min(nb, (p.N - 1) / 128);
+            if constexpr (SWIGLU)
+                nb = tl.n0 / 128;  // gate block; the up block is N/128 rows further
             const float *sb_ptr = tl.sbp + static_cast<int64_t>(nb) * p.ldsb;
+            const float *sbu_ptr = sb_ptr + static_cast<int64_t>(p.N / 128) * p.ldsb;
 
             float acc[CPW];
 #pragma unroll
@@ -444,7 +473,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
 
             // One K chunk: wait for its partial, read it from TMEM, release the
             // buffer, fold it into acc with the chunk's scales.
-            auto promote = [&](float sa_v, float sb_v) -> bool {
+            auto promote = [&](float sa_v, float sb_v, float sbu_v) -> bool {
                 const int b = c % NTMEM;
                 const uint32_t tph = (c / NTMEM) & 1;
                 const int s = c % STAGES;
@@ -456,16 +485,26 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                 if (!__all_sync(0xFFFFFFFFu, got))
                     return false;
                 tc_fence_after();
-                const uint32_t taddr = tmem_base + t_lane + b * BN + col0;
+                // TMEM column of 32-column piece pc of this thread's columns
+                auto pcol = [&](int pc) -> uint32_t {
+                    if constexpr (SWIGLU)
+                        return static_cast<uint32_t>(pc < 2 ? grp * 64 + pc * 32 : 128 + grp * 64 + (pc - 2) * 32);
+                    else
+                        return static_cast<uint32_t>(col0 + pc * 32);
+                };
+                const uint32_t tbase = tmem_base + t_lane + b * BN;
                 const float sc = sa_v * sb_v;
+                const float scu = SWIGLU ? sa_v * sbu_v : sc;  // up-block scale (SwiGLU)
+                (void)scu;
                 const float *sbr = sbrow_smem + s * BN + col0;
                 (void)sbr;
 
                 auto fold = [&](int pc, const uint32_t(&cur)[32]) {
                     if constexpr (BMODE == 0) {
+                        const float scp = (SWIGLU && pc >= 2) ? scu : sc;
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            acc[pc * 32 + j] = fmaf(sc, __uint_as_float(cur[j]), acc[pc * 32 + j]);
+                            acc[pc * 32 + j] = fmaf(scp, __uint_as_float(cur[j]), acc[pc * 32 + j]);
                     } else {
                         uint64_t sa2;
                         asm("mov.b64 %0, {%1, %1};" : "=l"(sa2) : "f"(sa_v));
@@ -489,22 +528,22 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                 uint32_t ra[32], rb[32];
                 if constexpr (NP == 2) {
                     // both loads in flight, one wait, release, then fold
-                    tmem_ld32(taddr, ra);
-                    tmem_ld32(taddr + 32, rb);
+                    tmem_ld32(tbase + pcol(0), ra);
+                    tmem_ld32(tbase + pcol(1), rb);
                     tmem_ld_wait_regs2(ra, rb);
                     release();
                     fold(0, ra);
                     fold(1, rb);
                 } else {
                     // four loads, each overlapped with the fold of the previous one
-                    tmem_ld32(taddr, ra);
+                    tmem_ld32(tbase + pcol(0), ra);
                     tmem_ld_wait_regs(ra);
 #pragma unroll
                     for (int pc = 0; pc < NP; ++pc) {
                         uint32_t(&cur)[32] = (pc & 1) ? rb : ra;
                         uint32_t(&nxt)[32] = (pc & 1) ? ra : rb;
                         if (pc + 1 < NP)
-                            tmem_ld32(taddr + (pc + 1) * 32, nxt);
+                            tmem_ld32(tbase + pcol(pc + 1), nxt);
                         fold(pc, cur);
                         if (pc + 1 < NP) {
                             tmem_ld_wait_regs(nxt);
@@ -527,67 +566,125 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
             // whole chunk pair to land and no register copy waits on it.
             auto ld_sa = [&](int kb) { return kb < num_kb ? __ldg(sa_ptr + static_cast<int64_t>(kb) * p.ldsa) : 0.0f; };
             auto ld_sb = [&](int kb) { return (BMODE == 0 && kb < num_kb) ? __ldg(sb_ptr + kb) : 0.0f; };
+            auto ld_sbu = [&](int kb) { return (SWIGLU && kb < num_kb) ? __ldg(sbu_ptr + kb) : 0.0f; };
             float sa0 = ld_sa(0), sb0 = ld_sb(0), sa1 = ld_sa(1), sb1 = ld_sb(1);
+            float su0 = ld_sbu(0), su1 = ld_sbu(1);
             int kb = 0;
             for (; kb + 1 < num_kb; kb += 2) {
-                if (!promote(sa0, sb0)) {
+                if (!promote(sa0, sb0, su0)) {
                     ok = false;
                     break;
                 }
                 sa0 = ld_sa(kb + 2);
                 sb0 = ld_sb(kb + 2);
-                if (!promote(sa1, sb1)) {
+                su0 = ld_sbu(kb + 2);
+                if (!promote(sa1, sb1, su1)) {
                     ok = false;
                     break;
                 }
                 sa1 = ld_sa(kb + 3);
                 sb1 = ld_sb(kb + 3);
+                su1 = ld_sbu(kb + 3);
             }
-            if (ok && kb < num_kb && !promote(sa0, sb0))
+            if (ok && kb < num_kb && !promote(sa0, sb0, su0))
                 ok = false;
             if (!ok)
                 break;
 
-            // ---------------------------------------------------------- epilogue
-            // Each round stages 32 rows x 64 bytes through this warp's 2 KB
-            // buffer (16-byte chunks XOR-swizzled by row pair, so that the
-            // row-wise writes and the row-contiguous read-back are both free
-            // of bank conflicts), then stores with row/column masks.
-            const int grow0 = tl.m0 + quarter * 32;
-            constexpr int COLS_PER_ROUND = OUT_F32 ? 16 : 32;
-            constexpr int ELEMS_PER_CHUNK = OUT_F32 ? 4 : 8;
+            if constexpr (SWIGLU) {
+                // ------------------------------------------------ SwiGLU + 1x128 quantisation
+                // h = silu(g) * u for this thread's 64 channels (acc[0..63] gate,
+                // acc[64..127] up), in FP32 with an IEEE divide
+                float am = 0.0f;
 #pragma unroll
-            for (int g = 0; g < CPW / COLS_PER_ROUND; ++g) {
+                for (int i = 0; i < 64; ++i) {
+                    const float g = acc[i];
+                    const float h = __fdiv_rn(g, 1.0f + expf(-g)) * acc[64 + i];
+                    acc[i] = h;
+                    am = fmaxf(am, fabsf(h));
+                }
+                // the row's other 64 channels belong to the other warpgroup
+                float *xch = reinterpret_cast<float *>(smem + L::OFF_XCH) + (tcount & 1) * 256;
+                xch[grp * 128 + row] = am;
+                mbar_arrive(bar_xch);
+                const bool got = mbar_wait(bar_xch, tcount & 1, ERR_TIMEOUT_CONSUMER);
+                if (!__all_sync(0xFFFFFFFFu, got)) {
+                    ok = false;
+                    break;
+                }
+                am = fmaxf(am, xch[(grp ^ 1) * 128 + row]);
+                const float scale = am == 0.0f ? 1.0f : __fdiv_rn(am, 448.0f);
+                // codes E4M3(h / scale), staged 32 rows x 64 bytes per warp
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float *a = &acc[g * COLS_PER_ROUND + j * ELEMS_PER_CHUNK];
-                    uint4 v;
-                    if constexpr (OUT_F32) {
-                        v = make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
-                                       __float_as_uint(a[3]));
-                    } else {
-                        v = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
-                                       pack_bf16x2(a[6], a[7]));
+                    uint32_t w[4];
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const float *h = &acc[j * 16 + q4 * 4];
+                        w[q4] = e4m3x2(__fdiv_rn(h[0], scale), __fdiv_rn(h[1], scale)) |
+                                (e4m3x2(__fdiv_rn(h[2], scale), __fdiv_rn(h[3], scale)) << 16);
                     }
-                    *reinterpret_cast<uint4 *>(epi + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)) = v;
+                    *reinterpret_cast<uint4 *>(epi + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
                 }
                 __syncwarp();
+                const int grow0 = tl.m0 + quarter * 32;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int idx = lane + 32 * i;
                     const int r = idx >> 2, j = idx & 3;
                     const uint4 v = *reinterpret_cast<const uint4 *>(epi + r * 64 + ((j ^ ((r >> 1) & 3)) * 16));
                     const int m = grow0 + r;
-                    const int n = tl.n0 + col0 + g * COLS_PER_ROUND + j * ELEMS_PER_CHUNK;
-                    if (m < tl.m_end && n < p.N) {
-                        const int64_t off = static_cast<int64_t>(m) * p.ldc + n;
-                        if constexpr (OUT_F32)
-                            *reinterpret_cast<uint4 *>(reinterpret_cast<float *>(p.C) + off) = v;
-                        else
-                            *reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.C) + off) = v;
-                    }
+                    if (m < tl.m_end)
+                        *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.C) + static_cast<int64_t>(m) * p.ldc +
+                                                   tl.n0 + grp * 64 + j * 16) = v;
                 }
                 __syncwarp();
+                if (grp == 0 && tl.m0 + row < tl.m_end)
+                    p.s_out[static_cast<int64_t>(tl.n0 / 128) * p.lds_out + tl.m0 + row] = scale;
+                ++tcount;
+            } else {
+                // ---------------------------------------------------------- epilogue
+                // Each round stages 32 rows x 64 bytes through this warp's 2 KB
+                // buffer (16-byte chunks XOR-swizzled by row pair, so that the
+                // row-wise writes and the row-contiguous read-back are both free
+                // of bank conflicts), then stores with row/column masks.
+                const int grow0 = tl.m0 + quarter * 32;
+                constexpr int COLS_PER_ROUND = OUT_F32 ? 16 : 32;
+                constexpr int ELEMS_PER_CHUNK = OUT_F32 ? 4 : 8;
+#pragma unroll
+                for (int g = 0; g < CPW / COLS_PER_ROUND; ++g) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float *a = &acc[g * COLS_PER_ROUND + j * ELEMS_PER_CHUNK];
+                        uint4 v;
+                        if constexpr (OUT_F32) {
+                            v = make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                                           __float_as_uint(a[3]));
+                        } else {
+                            v = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                                           pack_bf16x2(a[6], a[7]));
+                        }
+                        *reinterpret_cast<uint4 *>(epi + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)) = v;
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int idx = lane + 32 * i;
+                        const int r = idx >> 2, j = idx & 3;
+                        const uint4 v = *reinterpret_cast<const uint4 *>(epi + r * 64 + ((j ^ ((r >> 1) & 3)) * 16));
+                        const int m = grow0 + r;
+                        const int n = tl.n0 + col0 + g * COLS_PER_ROUND + j * ELEMS_PER_CHUNK;
+                        if (m < tl.m_end && n < p.N) {
+                            const int64_t off = static_cast<int64_t>(m) * p.ldc + n;
+                            if constexpr (OUT_F32)
+                                *reinterpret_cast<uint4 *>(reinterpret_cast<float *>(p.C) + off) = v;
+                            else
+                                *reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.C) + off) = v;
+                        }
+                    }
+                    __syncwarp();
+                }
             }
         }
     }

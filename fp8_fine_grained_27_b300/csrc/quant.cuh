@@ -146,13 +146,18 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p)
 //                   the row's 4 lanes; s[kb*lds + m].
 //   kBlock = true : one scale per 128x128 block, reduced over the CTA;
 //                   s[mb*lds + kb].
+// row_map (1x128 only, may be null): output row m reads input row
+// row_map[m] (a gather, e.g. tokens into expert order); a mapped row outside
+// [0, src_rows) reads as zeros.
 // Tile order: kb fastest, so neighbouring CTAs read neighbouring columns.
 // ---------------------------------------------------------------------------
 template <bool kBlock>
 __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t *__restrict__ x, int64_t M,
                                                               int64_t K, int64_t ldx,
                                                               uint8_t *__restrict__ q, int64_t ldq,
-                                                              float *__restrict__ s, int64_t lds)
+                                                              float *__restrict__ s, int64_t lds,
+                                                              const int32_t *__restrict__ row_map = nullptr,
+                                                              int64_t src_rows = 0)
 {
     __shared__ uint32_t red[kThreads / 32];
     const int tid = threadIdx.x;
@@ -169,9 +174,15 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t *__
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
             const int64_t m = m0 + rw + 64 * rr;
+            int64_t src = m;
+            bool ok = m < M;
+            if (!kBlock && row_map != nullptr && ok) {
+                src = row_map[m];
+                ok = src >= 0 && src < src_rows;
+            }
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                v[rr][i] = (m < M) ? ldg_stream(x + m * ldx + kb * 128 + (j + 4 * i) * 8) : make_uint4(0, 0, 0, 0);
+                v[rr][i] = ok ? ldg_stream(x + src * ldx + kb * 128 + (j + 4 * i) * 8) : make_uint4(0, 0, 0, 0);
         }
         uint32_t am[2];
 #pragma unroll

@@ -149,6 +149,86 @@ int fp8_grouped_gemm_moe(const uint8_t *A, int64_t lda, const float *sa, int64_t
                          int G, int64_t M_total, void *C, int64_t ldc, int out_dtype,
                          int64_t N, int64_t K, void *stream);
 
+/* ------------------------------------------------------------------------
+ * The routed-expert chain (V3 report §2 DeepSeekMoE: 256 routed experts, 8
+ * per token, SwiGLU experts; §4 aux-loss-free balancing: sigmoid affinity to
+ * each expert's centroid, top-k of affinity + bias, gates from the selected
+ * affinities normalised to sum 1).  One layer forward:
+ *   fp8_moe_route -> fp8_quant_1x128_gather -> fp8_grouped_gemm_moe_swiglu
+ *   -> fp8_grouped_gemm_moe (down projection) -> fp8_moe_combine.
+ * ------------------------------------------------------------------------ */
+
+/* Bytes of device workspace fp8_moe_route needs for E experts (-1 if E is
+ * outside 1 .. 1024). */
+int64_t fp8_moe_route_workspace_size(int E);
+
+/*
+ * fp8_moe_route -- routing and grouping of T tokens over E experts.
+ *   x          BF16 tokens [T][ldx], D used (D % 32 == 0).
+ *   centroids  FP32 [E][ldc]; bias FP32 [E] (selection only).
+ *   logits     out FP32 [T][E]: l[t][e] = sum_k x[t][k] * c[e][k], formed in
+ *              FP32 with one fused multiply-add per term in increasing k (the
+ *              decision below is taken from exactly these values).
+ *   expert_idx out int32 [T][topk]: the topk experts with the largest
+ *              1/(1+exp(-l)) + b (evaluated in double; a tie goes to the
+ *              lower index), listed in increasing expert order.
+ *   gate       out FP32 [T][topk]: s_e / (sum of the chosen s), s = the
+ *              double affinity, the sum taken in the listed order.
+ *   offsets    out int32 [E+1]: rows offsets[e] .. offsets[e+1]-1 belong to
+ *              expert e; rows of one expert hold its tokens in increasing
+ *              order.  token_of_row out int32 [T*topk]; row_of out int32
+ *              [T][topk] (row of token t's j-th listed expert).
+ *   workspace  device, >= fp8_moe_route_workspace_size(E) bytes, 256-byte
+ *              aligned, owned by the caller; contents on return unspecified.
+ *   Requires 1 <= E <= 1024, 1 <= topk <= min(E, 16).  T == 0 writes zero
+ *   offsets.  Deterministic: no result depends on launch timing.
+ */
+int fp8_moe_route(const void *x, int64_t T, int64_t D, int64_t ldx, const float *centroids, int64_t ldc,
+                  const float *bias, int E, int topk, float *logits, int32_t *expert_idx, float *gate,
+                  int32_t *offsets, int32_t *token_of_row, int32_t *row_of, void *workspace,
+                  int64_t workspace_bytes, void *stream);
+
+/*
+ * fp8_quant_1x128_gather -- fp8_quant_1x128 (along 0) of the rows
+ * x[row_map[r]], r = 0 .. R-1: gathering and quantising in one pass (equal,
+ * bit for bit, to quantising then gathering, since every scale belongs to
+ * one row).  x BF16 [T][ldx]; row_map DEVICE int32 [R]; q codes [R][ldq];
+ * s FP32 [K/128][lds], lds >= R.  A mapped row outside [0, T) quantises as
+ * zeros (codes 0, scale 1).  Requires K % 128 == 0.
+ */
+int fp8_quant_1x128_gather(const void *x, int64_t T, int64_t K, int64_t ldx, const int32_t *row_map, int64_t R,
+                           uint8_t *q, int64_t ldq, float *s, int64_t lds, void *stream);
+
+/*
+ * fp8_grouped_gemm_moe_swiglu -- per-expert up projection with the SwiGLU
+ * and its 1x128 quantisation fused into the epilogue (the down projection
+ * takes FP8 inputs, V3 report §6).
+ *   A, sa, group_offsets, G, M_total as fp8_grouped_gemm_moe.
+ *   B   codes [G][2*Nh][K]: rows 0 .. Nh-1 the gate projection, Nh .. 2Nh-1
+ *       the up projection; sb FP32 [G][2*Nh/128][K/128] block scales.
+ *   For each row and channel n < Nh, with g and u the FP32 results of the
+ *   block-scaled GEMM (as fp8_gemm_blockscaled computes them) for rows n
+ *   and Nh + n of B:  h = g / (1 + expf(-g)) * u  (FP32, IEEE divide), and
+ *   h is quantised in 1x128 tiles along n: Q codes [M_total][ldq],
+ *   s FP32 [Nh/128][lds], lds >= M_total (s = amax/448, codes of the IEEE
+ *   quotient h / s).  Rows of empty experts and rows past offs[G] are not
+ *   written.  Requires Nh % 128 == 0, K % 128 == 0, 1 <= G <= 1024.
+ */
+int fp8_grouped_gemm_moe_swiglu(const uint8_t *A, int64_t lda, const float *sa, int64_t ldsa,
+                                const uint8_t *B, const float *sb, const int32_t *group_offsets, int G,
+                                int64_t M_total, uint8_t *Q, int64_t ldq, float *s, int64_t lds,
+                                int64_t Nh, int64_t K, void *stream);
+
+/*
+ * fp8_moe_combine -- out[t][n] = BF16_RNE(sum_j gate[t][j] * Y[row_of[t][j]][n]),
+ * the sum formed in FP32 with one fused multiply-add per listed expert, in
+ * list order.  Y BF16 [R][ldy] (the down projection's rows); row_of int32
+ * [T][topk]; gate FP32 [T][topk]; out BF16 [T][ldo].  A row index outside
+ * [0, R) contributes nothing.  Requires N % 8 == 0.
+ */
+int fp8_moe_combine(const void *Y, int64_t ldy, int64_t R, const int32_t *row_of, const float *gate, int64_t T,
+                    int topk, int64_t N, void *out, int64_t ldo, void *stream);
+
 /*
  * fp8bs_e4m3_encode -- element-wise q[i] = E4M3_RNE_saturate(x[i]) with the
  * same conversion the quantisers use; x FP32 [n], q uint8 [n] (device).
