@@ -147,6 +147,11 @@ def workload_desc(name):
                   "gemms": 1, "quant": "dY, X 1x128 along tokens (transposed)", "out": "fp32"},
         "dgrad": {"workload": "dgrad_ffn", "M": 16384, "K": 18432, "N": [7168], "gemms": 1,
                   "quant": "dY 1x128, W 128x128 written transposed (codes + scales)", "out": "bf16"},
+        "moe_chain": {"workload": "moe_layer_forward", "M": 32768, "K": [7168, 2048], "N": [4096, 7168],
+                      "tokens": 4096, "experts": 256, "topk": 8,
+                      "gemms": "2 grouped (up 2x2048 with fused SwiGLU + 1x128 quantise; down 7168)",
+                      "quant": "gathered token rows 1x128 (weights pre-quantised)",
+                      "other": "routing (FP32 logits, top-8, grouping), combine", "out": "bf16"},
         "moe": {"workload": "moe_grouped_up", "M": 32768, "K": 7168, "N": [4096], "experts": 256,
                 "topk": 8, "gemms": 1, "quant": "grouped rows 1x128 (weights pre-quantised)", "out": "bf16"},
         "tiny": {"workload": "tiny", "M": 128, "K": 512, "N": [256], "gemms": 1,
@@ -154,8 +159,14 @@ def workload_desc(name):
     }[name]
 
 
+# kernels one labelled C-ABI call launches (fp8_moe_route: logits, selection, grouping)
+KERNELS_PER_CALL = {"route": 3}
+
+
 def gemm_flops(name):
     d = workload_desc(name)
+    if name == "moe_chain":
+        return sum(2.0 * d["M"] * n * k for n, k in zip(d["N"], d["K"]))
     return sum(2.0 * d["M"] * n * d["K"] for n in d["N"])
 
 
@@ -174,6 +185,8 @@ def quant_bytes(name):
         return d["M"] * d["K"] * (3 + 4 / 128) + d["K"] * d["N"][0] * (3 + 4 / (128 * 128))
     if name == "moe":
         return d["M"] * d["K"] * (3 + 4 / 128)
+    if name == "moe_chain":
+        return d["M"] * d["K"][0] * (3 + 4 / 128)
     raise KeyError(name)
 
 
@@ -198,6 +211,9 @@ class Step:
         elif name == "dgrad":
             d = synth.dgrad(seed=seed)
             self.host = {"dY": d["dY"], "W": d["W"]}
+        elif name == "moe_chain":
+            cent, bias = synth.moe_router(seed=seed)
+            self.host = {"X": synth.moe_tokens(seed=seed), "cent": cent, "bias": bias}
         elif name == "moe":
             tok = synth.moe_tokens(seed=seed)
             offs, token_of_row = synth.moe_route(tok, seed=seed)
@@ -231,6 +247,40 @@ class Step:
             self.d["qwt"] = torch.empty((Ci, Co), dtype=torch.uint8, device="cuda")
             self.d["swt"] = torch.empty((Ci // 128, (Co + 127) // 128), dtype=torch.float32, device="cuda")
             self.d["C"] = [torch.empty((T, Ci), dtype=torch.bfloat16, device="cuda")]
+        elif name == "moe_chain":
+            T, D = self.host["X"].shape
+            E, k, Nh = 256, 8, 2048
+            R = T * k
+            self.d["X"] = dev(self.host["X"])
+            self.d["cent"] = torch.from_numpy(np.ascontiguousarray(self.host["cent"].T)).cuda()  # k-major
+            self.d["bias"] = torch.from_numpy(self.host["bias"]).cuda()
+            self.d["route"] = {
+                "logits": torch.empty((T, E), dtype=torch.float32, device="cuda"),
+                "expert_idx": torch.empty((T, k), dtype=torch.int32, device="cuda"),
+                "gate": torch.empty((T, k), dtype=torch.float32, device="cuda"),
+                "offsets": torch.empty(E + 1, dtype=torch.int32, device="cuda"),
+                "token_of_row": torch.empty(R, dtype=torch.int32, device="cuda"),
+                "row_of": torch.empty((T, k), dtype=torch.int32, device="cuda")}
+            self.d["ws"] = torch.empty(max(fb.lib().fp8_moe_route_workspace_size(E), 256), dtype=torch.uint8,
+                                       device="cuda")
+            self.d["qa"] = torch.empty((R, D), dtype=torch.uint8, device="cuda")
+            self.d["sa"] = torch.empty((D // 128, R), dtype=torch.float32, device="cuda")
+            self.d["h"] = torch.empty((R, Nh), dtype=torch.uint8, device="cuda")
+            self.d["sh"] = torch.empty((Nh // 128, R), dtype=torch.float32, device="cuda")
+            self.d["Y"] = torch.empty((R, D), dtype=torch.bfloat16, device="cuda")
+            self.d["qwu"] = torch.empty((E, 2 * Nh, D), dtype=torch.uint8, device="cuda")
+            self.d["swu"] = torch.empty((E, 2 * Nh // 128, D // 128), dtype=torch.float32, device="cuda")
+            self.d["qwd"] = torch.empty((E, D, Nh), dtype=torch.uint8, device="cuda")
+            self.d["swd"] = torch.empty((E, D // 128, Nh // 128), dtype=torch.float32, device="cuda")
+            for e0 in range(0, E, 16):  # expert weights: quantised once, outside the step
+                w = dev(synth.moe_weights("up", e0, e0 + 16, seed=seed))
+                fb.quant_128x128(w.view(-1, D), q=self.d["qwu"][e0:e0 + 16].view(-1, D),
+                                 s=self.d["swu"][e0:e0 + 16].view(-1, D // 128))
+                w = dev(synth.moe_weights("down", e0, e0 + 16, seed=seed))
+                fb.quant_128x128(w.view(-1, Nh), q=self.d["qwd"][e0:e0 + 16].view(-1, Nh),
+                                 s=self.d["swd"][e0:e0 + 16].view(-1, Nh // 128))
+                del w
+            self.d["C"] = [torch.empty((T, D), dtype=torch.bfloat16, device="cuda")]
         elif name == "moe":
             self.d["A"] = dev(self.host["A"])
             M, K = self.host["A"].shape
@@ -267,6 +317,16 @@ class Step:
             return [("quant_1x128", lambda: fb.quant_1x128(d["dY"], q=d["qdy"], s=d["sdy"])),
                     ("quant_128x128_t", lambda: fb.quant_128x128_t(d["W"], straight=False, qt=d["qwt"], st=d["swt"])),
                     ("gemm", lambda: fb.gemm_blockscaled(d["qdy"], d["sdy"], d["qwt"], d["swt"], 0, C=d["C"][0]))]
+        if self.name == "moe_chain":
+            r = d["route"]
+            return [("route", lambda: fb.moe_route(d["X"], d["cent"], d["bias"], 8, out=r, workspace=d["ws"])),
+                    ("quant_1x128_gather", lambda: fb.quant_1x128_gather(d["X"], r["token_of_row"], q=d["qa"],
+                                                                         s=d["sa"])),
+                    ("gemm_up_swiglu", lambda: fb.grouped_gemm_moe_swiglu(d["qa"], d["sa"], d["qwu"], d["swu"],
+                                                                          r["offsets"], Q=d["h"], s=d["sh"])),
+                    ("gemm_down", lambda: fb.grouped_gemm_moe(d["h"], d["sh"], d["qwd"], d["swd"], r["offsets"],
+                                                              C=d["Y"])),
+                    ("combine", lambda: fb.moe_combine(d["Y"], r["row_of"], r["gate"], out=d["C"][0]))]
         if self.name == "moe":
             return [("quant_1x128", lambda: fb.quant_1x128(d["A"], q=d["qa"], s=d["sa"])),
                     ("gemm", lambda: fb.grouped_gemm_moe(d["qa"], d["sa"], d["qb"], d["sb"], d["offs"],
@@ -281,6 +341,8 @@ class Step:
             return [("dY", self.host["dY"]), ("X", self.host["X"])]
         if self.name == "dgrad":
             return [("dY", self.host["dY"]), ("W", self.host["W"])]
+        if self.name == "moe_chain":
+            return [("X", self.host["X"])]
         return [("A", self.host["A"])]
 
 
@@ -361,9 +423,9 @@ def run_ours(args, rank, world):
     peaks, peaks_src = load_peaks()
     fp8_peak = 2.0 * peaks["bf16_tflops"]
     # GEMM launches of one step (there may be several): their summed mean duration
-    g_idx = [j for j, (l, _) in enumerate(launches) if l == "gemm"]
+    g_idx = [j for j, (l, _) in enumerate(launches) if l.startswith("gemm")]
     gemm_ms = float(np.mean([sum(ev[k][j].elapsed_time(ev[k][j + 1]) for j in g_idx) for k in range(args.steps)]))
-    q_idx = [j for j, (l, _) in enumerate(launches) if l != "gemm"]
+    q_idx = [j for j, (l, _) in enumerate(launches) if l.startswith("quant")]
     quant_ms = float(np.mean([sum(ev[k][j].elapsed_time(ev[k][j + 1]) for j in q_idx) for k in range(args.steps)]))
     achieved = flops / (gemm_ms * 1e-3) / 1e12
     quant_gbs = qbytes / (quant_ms * 1e-3) / 1e9
@@ -393,7 +455,7 @@ def run_ours(args, rank, world):
                   "bytes_per_step": int(qbytes)},
         "per_kernel_ms": {l: round(float(np.mean(v)), 5) for l, v in per_kernel.items()},
         "e2e": e2e,
-        "gpu_launches": nk * args.steps,
+        "gpu_launches": sum(KERNELS_PER_CALL.get(l, 1) for l, _ in launches) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": round(t1 - t0, 3),
         "cpu_baseline": cpu,
@@ -417,6 +479,8 @@ def run_e2e(args, step, torch, fb, launches, flops, world, dist):
         targets = {"dY": step.d["dY"], "X": step.d["X"]}
     elif step.name == "dgrad":
         targets = {"dY": step.d["dY"], "W": step.d["W"]}
+    elif step.name == "moe_chain":
+        targets = {"X": step.d["X"]}
     else:
         targets = {"A": step.d["A"]}
     h2d = sum(p.numel() * p.element_size() for _, p in pinned)
@@ -493,6 +557,25 @@ def oracle_sample(workload, seed=0):
             _, _, qwt, swt = oracle.quant_128x128_t(W)
             oracle.gemm_blockscaled(qd, sd, qwt, swt, 0)
         return work, 2.0 * 16 * 2048 * 18432, "16 rows x 2048 columns of dX (K = 18432), with their quantisation"
+    if workload == "moe_chain":
+        tok = synth.moe_tokens(seed=seed)[:1]
+        cent, bias = synth.moe_router(seed=seed)
+
+        def work():
+            l = oracle.route_logits(tok, cent)
+            sel, gate = oracle.route_select(l, bias, 8)
+            ys = []
+            for t in range(tok.shape[0]):
+                qa, sa = oracle.quant_1x128_rows(np.ascontiguousarray(np.repeat(tok[t:t + 1], 8, axis=0)))
+                for j, e in enumerate(sel[t]):
+                    qu, su = oracle.quant_128x128(synth.moe_weights("up", int(e), int(e) + 1, seed=seed)[0])
+                    h, sh = oracle.swiglu_quant(oracle.gemm_blockscaled(qa[j:j + 1], sa[:, j:j + 1], qu, su, 0))
+                    qd, sd = oracle.quant_128x128(synth.moe_weights("down", int(e), int(e) + 1, seed=seed)[0])
+                    ys.append(oracle.bf16_round(oracle.gemm_blockscaled(h, sh, qd, sd, 0)))
+            oracle.moe_combine(np.concatenate(ys), np.arange(len(ys), dtype=np.int32).reshape(-1, 8), gate)
+        flops = 1 * 8 * (2.0 * 4096 * 7168 + 2.0 * 7168 * 2048)
+        return work, flops, ("1 of 4096 tokens through the layer (routing over all 256 experts, each token's "
+                             "8 experts' weight quantisation, up GEMM + SwiGLU, down GEMM, combine)")
     if workload == "moe":
         tok = synth.moe_tokens(seed=seed, T=64)
         W = synth.moe_weights("up", 0, 1, seed=seed)[0][:1024]
@@ -554,7 +637,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
-    ap.add_argument("--workload", default="mla", choices=["mla", "ffn", "wgrad", "dgrad", "moe", "tiny"])
+    ap.add_argument("--workload", default="mla", choices=["mla", "ffn", "wgrad", "dgrad", "moe", "moe_chain", "tiny"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
@@ -568,7 +651,8 @@ def main():
         args.warmup = args.warmup if args.warmup is not None else 1
         run_reference(args, rank, world)
         return
-    default_steps = {"mla": 10000, "tiny": 10000, "ffn": 200, "wgrad": 1000, "dgrad": 200, "moe": 300}[args.workload]
+    default_steps = {"mla": 10000, "tiny": 10000, "ffn": 200, "wgrad": 1000, "dgrad": 200, "moe": 300,
+                     "moe_chain": 200}[args.workload]
     args.steps = args.steps or default_steps
     args.warmup = max(3, args.warmup if args.warmup is not None else 20)
     run_ours(args, rank, world)

@@ -180,13 +180,14 @@ def get_device_error(stream=None) -> int:
     return lib().fp8bs_get_device_error(_stream(stream))
 
 
-def moe_route(x: torch.Tensor, centroids: torch.Tensor, bias: torch.Tensor, topk: int, out=None,
+def moe_route(x: torch.Tensor, centroids_t: torch.Tensor, bias: torch.Tensor, topk: int, out=None,
               workspace=None, stream=None):
-    """Routing of BF16 tokens x [T, D] over E experts (centroids f32 [E, D], bias f32 [E]).
+    """Routing of BF16 tokens x [T, D] over E experts (centroids k-major f32 [D, E], bias f32 [E]).
     Returns a dict of device tensors: logits [T, E], expert_idx [T, k], gate [T, k],
     offsets [E+1], token_of_row [T*k], row_of [T, k] (int32 / f32)."""
     T, D = x.shape
-    E = centroids.shape[0]
+    E = centroids_t.shape[1]
+    centroids = centroids_t
     dev = x.device
     o = out if out is not None else {
         "logits": torch.empty((T, E), dtype=torch.float32, device=dev),

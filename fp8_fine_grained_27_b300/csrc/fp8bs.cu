@@ -513,9 +513,10 @@ int fp8_moe_route(const void *x, int64_t T, int64_t D, int64_t ldx, const float 
                   int32_t *offsets, int32_t *token_of_row, int32_t *row_of, void *workspace,
                   int64_t workspace_bytes, void *stream)
 {
-    if (T < 0 || D <= 0 || E < 1 || E > moe::kMaxExperts || topk < 1 || topk > moe::kMaxTopk || topk > E)
+    if (T < 0 || D <= 0 || E < 1 || E > moe::kMaxExperts || E % 4 != 0 || topk < 1 || topk > moe::kMaxTopk ||
+        topk > E)
         return FP8BS_EINVAL;
-    if (D % 32 != 0 || ldx < D || ldc < D || !offsets || !workspace ||
+    if (D % 32 != 0 || ldx < D || ldc < E || !offsets || !workspace ||
         workspace_bytes < fp8_moe_route_workspace_size(E))
         return FP8BS_EINVAL;
     if (T > 0 && (!x || !centroids || !bias || !logits || !expert_idx || !gate || !token_of_row || !row_of))
@@ -536,7 +537,7 @@ int fp8_moe_route(const void *x, int64_t T, int64_t D, int64_t ldx, const float 
             return FP8BS_ECUDA;
     } else {
         const dim3 lg(static_cast<unsigned>((T + moe::kLT - 1) / moe::kLT), (E + moe::kLE - 1) / moe::kLE);
-        moe::route_logits_kernel<<<lg, 256, 0, st>>>(static_cast<const uint16_t *>(x), T, D, ldx, centroids, ldc, E,
+        moe::route_logits_kernel<<<lg, 64, 0, st>>>(static_cast<const uint16_t *>(x), T, D, ldx, centroids, ldc, E,
                                                      logits, counts);
         const unsigned sg = static_cast<unsigned>((T + 7) / 8);
         if (E <= 256)

@@ -26,103 +26,233 @@ constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopk = 16;
 
 // ---------------------------------------------------------------------------
-// Logits: a 64-token x 64-expert tile per CTA, 256 threads, 4 x 4 outputs per
-// thread.  K advances 32 at a time through shared memory (tokens converted
-// from BF16); every output accumulates its terms in increasing k with fmaf.
+// Logits: a 64-token x 64-expert tile per CTA of 64 threads; a thread owns 8
+// tokens x 8 experts (two groups of four, 32 apart, so that every shared-
+// memory read of a warp is one wavefront).  Every output accumulates its
+// terms in increasing k, one fused multiply-add per term.  The multiply-adds
+// run two outputs at a time (fma.rn.f32x2: each lane is an ordinary fmaf),
+// pairing (t, e) with (t+1, e+1) and (t, e+1) with (t+1, e), so both
+// operands are contiguous pairs in shared memory (one half-swap of the
+// expert pair).  The problem gives few threads (one per 64 outputs), so each
+// warp keeps 32 independent multiply-adds per step and reads the next
+// step's operands during the current one.  K advances 32 at a time through
+// double-buffered shared memory: the centroids (k-major) by cp.async, the
+// tokens through registers, converted from BF16 and transposed.
 // Requires D % 32 == 0.
 // ---------------------------------------------------------------------------
-constexpr int kLT = 64, kLE = 64, kLK = 32, kLPad = 4;
+constexpr int kLT = 64, kLE = 64, kLK = 32;
+constexpr int kXP = kLT + 4;  // row pitch of the token tile (floats)
+constexpr int kCP = kLE + 4;  // row pitch of the centroid tile
 
-__global__ void __launch_bounds__(256) route_logits_kernel(const uint16_t *__restrict__ x, int64_t T, int64_t D,
-                                                           int64_t ldx, const float *__restrict__ cent,
-                                                           int64_t ldc, int E, float *__restrict__ logits,
-                                                           int *__restrict__ counts)
+__device__ __forceinline__ uint64_t swap_halves(uint64_t v)
 {
-    __shared__ __align__(16) float xs[kLK][kLT + kLPad];
-    __shared__ __align__(16) float cs[kLK][kLE + kLPad];
+    uint32_t lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(v));
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(hi), "r"(lo));
+    return r;
+}
+
+__device__ __forceinline__ void fma2(uint64_t &acc, uint64_t a, uint64_t b)
+{
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
+__device__ __forceinline__ void lds2(uint64_t &a, uint64_t &b, uint32_t addr)
+{
+    asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr) : "memory");
+}
+
+__global__ void __launch_bounds__(64) route_logits_kernel(const uint16_t *__restrict__ x, int64_t T, int64_t D,
+                                                          int64_t ldx, const float *__restrict__ centT, int64_t ldc,
+                                                          int E, float *__restrict__ logits, int *__restrict__ counts)
+{
+    __shared__ __align__(16) float xs[2][kLK][kXP];
+    __shared__ __align__(16) float cs[2][kLK][kCP];
     const int tid = threadIdx.x;
-    const int ty = tid >> 4, tx = tid & 15;
+    const int tx = tid & 7, ty = tid >> 3;  // experts {4tx, 32+4tx} + 0..3, tokens {4ty, 32+4ty} + 0..3
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kLT;
     const int e0 = blockIdx.y * kLE;
     if (blockIdx.x == 0 && blockIdx.y == 0)
-        for (int e = tid; e < E; e += 256)
+        for (int e = tid; e < E; e += 64)
             counts[e] = 0;  // the selection kernel, next on the stream, counts into it
 
-    // loader mapping: tokens: row tid/4, 8 k from (tid%4)*8; centroids: expert
-    // tid/8 (+32), 4 k from (tid%8)*4
-    const int xr = tid >> 2, xk = (tid & 3) * 8;
-    const int cr = tid >> 3, ck = (tid & 7) * 4;
-    const bool xok = t0 + xr < T;
-    const bool cok0 = e0 + cr < E, cok1 = e0 + cr + 32 < E;
-    const uint16_t *xp = x + (t0 + xr) * ldx + xk;
-    const float *cp0 = cent + static_cast<int64_t>(e0 + cr) * ldc + ck;
-    const float *cp1 = cent + static_cast<int64_t>(e0 + cr + 32) * ldc + ck;
-
-    float acc[4][4];
+    // token loader: row tid, 32 BF16 of K per chunk
+    const bool xok = t0 + tid < T;
+    const uint16_t *xp = x + (t0 + tid) * ldx;
+    uint4 xv[4];
+    auto fetch_x = [&](int64_t k0) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            acc[i][j] = 0.0f;
-
-    uint4 xv = xok ? *reinterpret_cast<const uint4 *>(xp) : make_uint4(0, 0, 0, 0);
-    float4 c0 = cok0 ? *reinterpret_cast<const float4 *>(cp0) : make_float4(0, 0, 0, 0);
-    float4 c1 = cok1 ? *reinterpret_cast<const float4 *>(cp1) : make_float4(0, 0, 0, 0);
-    for (int64_t k0 = 0; k0 < D; k0 += kLK) {
-        __syncthreads();  // the previous chunk's reads are done
-        const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
+        for (int i = 0; i < 4; ++i)
+            xv[i] = xok ? *reinterpret_cast<const uint4 *>(xp + k0 + 8 * i) : make_uint4(0, 0, 0, 0);
+    };
+    auto stage_x = [&](int b) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            xs[xk + 2 * i][xr] = __uint_as_float(w[i] << 16);
-            xs[xk + 2 * i + 1][xr] = __uint_as_float(w[i] & 0xFFFF0000u);
+            const uint32_t w[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                xs[b][8 * i + 2 * j][tid] = __uint_as_float(w[j] << 16);
+                xs[b][8 * i + 2 * j + 1][tid] = __uint_as_float(w[j] & 0xFFFF0000u);
+            }
         }
-        cs[ck + 0][cr] = c0.x;
-        cs[ck + 1][cr] = c0.y;
-        cs[ck + 2][cr] = c0.z;
-        cs[ck + 3][cr] = c0.w;
-        cs[ck + 0][cr + 32] = c1.x;
-        cs[ck + 1][cr + 32] = c1.y;
-        cs[ck + 2][cr + 32] = c1.z;
-        cs[ck + 3][cr + 32] = c1.w;
-        __syncthreads();
-        if (k0 + kLK < D) {  // next chunk's loads overlap this chunk's FMAs
-            xv = xok ? *reinterpret_cast<const uint4 *>(xp + k0 + kLK) : make_uint4(0, 0, 0, 0);
-            c0 = cok0 ? *reinterpret_cast<const float4 *>(cp0 + k0 + kLK) : make_float4(0, 0, 0, 0);
-            c1 = cok1 ? *reinterpret_cast<const float4 *>(cp1 + k0 + kLK) : make_float4(0, 0, 0, 0);
+    };
+    // centroid loader: 32 rows of K x 16 chunks of 16 bytes (4 experts) per chunk of K;
+    // thread: chunk tid % 16 of rows tid / 16 + 4 i
+    const int cc = tid & 15, cr = tid >> 4;
+    const bool cok = e0 + 4 * cc < E;  // E % 4 == 0: a chunk is wholly in or out
+    auto fetch_c = [&](int64_t k0, int b) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = cr + 4 * i;
+            const float *src = centT + (k0 + r) * ldc + (cok ? e0 + 4 * cc : 0);
+            cp_async16_zfill(smem_addr(&cs[b][r][4 * cc]), src, cok ? 16u : 0u);
         }
-#pragma unroll 8
+    };
+
+    // accd[p][q] = {out(tp, eq), out(tp+1, eq+1)}, accx[p][q] = {out(tp, eq+1), out(tp+1, eq)}
+    // for token pair p (tp = 4ty + 2p, p < 2; 32 + 4ty + 2(p-2), p >= 2) and expert pair q likewise
+    uint64_t accd[4][4], accx[4][4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            accd[p][q] = accx[p][q] = 0;
+
+    fetch_c(0, 0);
+    fetch_x(0);
+    stage_x(0);
+    cp_async_wait_all();
+    __syncthreads();
+    int b = 0;
+    for (int64_t k0 = 0; k0 < D; k0 += kLK) {
+        const bool more = k0 + kLK < D;
+        if (more) {  // the next chunk lands while this one is multiplied
+            fetch_c(k0 + kLK, b ^ 1);
+            fetch_x(k0 + kLK);
+        }
+        const uint32_t xa = smem_addr(&xs[b][0][4 * ty]), ca = smem_addr(&cs[b][0][4 * tx]);
+        uint64_t a[4], c[4];
+        lds2(a[0], a[1], xa);
+        lds2(a[2], a[3], xa + 128);
+        lds2(c[0], c[1], ca);
+        lds2(c[2], c[3], ca + 128);
+#pragma unroll
         for (int kk = 0; kk < kLK; ++kk) {
-            const float4 a = *reinterpret_cast<const float4 *>(&xs[kk][ty * 4]);
-            const float4 b = *reinterpret_cast<const float4 *>(&cs[kk][tx * 4]);
-            const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+            uint64_t an[4], cn[4];
+            if (kk + 1 < kLK) {
+                const uint32_t xo = xa + (kk + 1) * kXP * 4, co = ca + (kk + 1) * kCP * 4;
+                lds2(an[0], an[1], xo);
+                lds2(an[2], an[3], xo + 128);
+                lds2(cn[0], cn[1], co);
+                lds2(cn[2], cn[3], co + 128);
+            }
+            uint64_t cw[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int q = 0; q < 4; ++q)
+                cw[q] = swap_halves(c[q]);
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
+            for (int p = 0; p < 4; ++p)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    fma2(accd[p][q], a[p], c[q]);
+                    fma2(accx[p][q], a[p], cw[q]);
+                }
+            if (kk + 1 < kLK) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    a[i] = an[i];
+                    c[i] = cn[i];
+                }
+            }
         }
+        if (more)
+            stage_x(b ^ 1);
+        cp_async_wait_all();
+        __syncthreads();
+        b ^= 1;
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int64_t t = t0 + ty * 4 + i;
-        if (t >= T)
-            continue;
+    for (int p = 0; p < 4; ++p)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = e0 + tx * 4 + j;
-            if (e < E)
-                logits[t * E + e] = acc[i][j];
+        for (int q = 0; q < 4; ++q) {
+            float d0, d1, x0, x1;
+            asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(accd[p][q]));
+            asm("mov.b64 {%0, %1}, %2;" : "=f"(x0), "=f"(x1) : "l"(accx[p][q]));
+            const int64_t ta = t0 + (p < 2 ? 4 * ty + 2 * p : 32 + 4 * ty + 2 * (p - 2)), tb = ta + 1;
+            const int ea = e0 + (q < 2 ? 4 * tx + 2 * q : 32 + 4 * tx + 2 * (q - 2)), eb = ea + 1;
+            if (ta < T && ea < E)
+                logits[ta * E + ea] = d0;
+            if (tb < T && eb < E)
+                logits[tb * E + eb] = d1;
+            if (ta < T && eb < E)
+                logits[ta * E + eb] = x0;
+            if (tb < T && ea < E)
+                logits[tb * E + ea] = x1;
         }
-    }
 }
 
 // affinity of a logit: 1 / (1 + exp(-l)) in double
 __device__ __forceinline__ double affinity(float l) { return 1.0 / (1.0 + exp(-static_cast<double>(l))); }
 
+// The selection key s + b is defined in double.  An FP32 screen decides
+// almost every token: with CUDA's expf within 2 ulp, 1 + e and the divide
+// correctly rounded and |b| < 4, the FP32 key is within 2^-20 of the exact
+// key, so when the k-th and (k+1)-th FP32 keys are more than kScreenGap
+// apart the FP32 top-k is the exact top-k (and the double one).  Tokens
+// closer than that are decided again from the double keys.
+constexpr float kScreenGap = 0x1p-16f;
+
+// warp arg-max over (key desc, index asc)
+template <typename F>
+__device__ __forceinline__ void warp_argmax(F &bk, int &bi)
+{
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const F ok = __shfl_xor_sync(0xFFFFFFFFu, bk, o);
+        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+        if (ok > bk || (ok == bk && oi < bi)) {
+            bk = ok;
+            bi = oi;
+        }
+    }
+}
+
+// k rounds of arg-max over this lane's NJ keys; returns the k-th key and the
+// (k+1)-th (or -inf when every expert is chosen); chosen[] in pick order.
+template <int NJ, typename F>
+__device__ __forceinline__ void top_k(const F (&key)[NJ], int lane, int E, int topk, int *chosen, F &kth, F &next)
+{
+    uint32_t taken = 0;
+    kth = next = -INFINITY;
+#pragma unroll 1
+    for (int r = 0; r <= topk && r < E; ++r) {
+        F bk = -INFINITY;
+        int bi = 0x7FFFFFFF;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            const int e = lane + 32 * j;
+            if (e < E && !((taken >> j) & 1u) && (key[j] > bk || bi == 0x7FFFFFFF)) {
+                bk = key[j];
+                bi = e;
+            }
+        }
+        warp_argmax(bk, bi);
+        if (r == topk) {
+            next = bk;
+            break;
+        }
+        if ((bi & 31) == lane)
+            taken |= 1u << (bi >> 5);
+        chosen[r] = bi;
+        kth = bk;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Selection: one warp per token; lane i holds experts i, i + 32, ... (NJ per
-// lane).  k rounds of a warp arg-max over (key desc, index asc) pick the
-// experts; they are listed in increasing index order with their gates.
+// lane).  The chosen experts are listed in increasing index order with
+// their gates (double affinities, summed in that order).
 // ---------------------------------------------------------------------------
 template <int NJ>
 __global__ void __launch_bounds__(256) route_select_kernel(const float *__restrict__ logits, int64_t T, int E,
@@ -135,58 +265,47 @@ __global__ void __launch_bounds__(256) route_select_kernel(const float *__restri
     if (t >= T)
         return;
     const float *lt = logits + t * E;
-    double key[NJ];
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-        const int e = lane + 32 * j;
-        key[j] = (e < E) ? affinity(lt[e]) + static_cast<double>(bias[e]) : -1.0e300;
-    }
-    uint32_t taken = 0;
     int chosen[kMaxTopk];
-#pragma unroll 1
-    for (int r = 0; r < topk; ++r) {
-        double bk = -1.0e308;
-        int bi = 0x7FFFFFFF;
+    {
+        float key[NJ];
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
             const int e = lane + 32 * j;
-            if (e < E && !((taken >> j) & 1u) && key[j] > bk) {
-                bk = key[j];
-                bi = e;
-            }
+            key[j] = (e < E) ? __fdiv_rn(1.0f, 1.0f + expf(-lt[e])) + bias[e] : -INFINITY;
         }
+        float kth, next;
+        top_k(key, lane, E, topk, chosen, kth, next);
+        if (!(kth - next > kScreenGap)) {  // near tie: decide from the double keys
+            double dkey[NJ];
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-            const double ok = __shfl_xor_sync(0xFFFFFFFFu, bk, o);
-            const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-            if (ok > bk || (ok == bk && oi < bi)) {
-                bk = ok;
-                bi = oi;
+            for (int j = 0; j < NJ; ++j) {
+                const int e = lane + 32 * j;
+                dkey[j] = (e < E) ? affinity(lt[e]) + static_cast<double>(bias[e]) : -INFINITY;
             }
+            double dk, dn;
+            top_k(dkey, lane, E, topk, chosen, dk, dn);
         }
-        if ((bi & 31) == lane)
-            taken |= 1u << (bi >> 5);
-        chosen[r] = bi;
     }
-    if (lane == 0) {
-        // increasing expert order (insertion sort of at most 16 indices)
-        for (int i = 1; i < topk; ++i) {
-            const int v = chosen[i];
-            int j = i - 1;
-            while (j >= 0 && chosen[j] > v) {
-                chosen[j + 1] = chosen[j];
-                --j;
-            }
-            chosen[j + 1] = v;
+    // lanes 0 .. topk-1 hold one chosen expert each, in increasing order
+    int mine = 0x7FFFFFFF;
+    for (int i = 0; i < topk; ++i) {  // rank of chosen[lane] among the chosen
+        const int v = chosen[i];
+        if (lane < topk) {
+            int rank = 0;
+            for (int q = 0; q < topk; ++q)
+                rank += chosen[q] < v;
+            if (rank == lane)
+                mine = v;
         }
-        double sum = 0.0;
-        for (int i = 0; i < topk; ++i)
-            sum += affinity(lt[chosen[i]]);
-        for (int i = 0; i < topk; ++i) {
-            sel[t * topk + i] = chosen[i];
-            gate[t * topk + i] = static_cast<float>(affinity(lt[chosen[i]]) / sum);
-            atomicAdd(&counts[chosen[i]], 1);
-        }
+    }
+    const double s_mine = (lane < topk) ? affinity(lt[mine]) : 0.0;
+    double sum = 0.0;
+    for (int i = 0; i < topk; ++i)
+        sum += __shfl_sync(0xFFFFFFFFu, s_mine, i);
+    if (lane < topk) {
+        sel[t * topk + lane] = mine;
+        gate[t * topk + lane] = static_cast<float>(s_mine / sum);
+        atomicAdd(&counts[mine], 1);
     }
 }
 

@@ -165,8 +165,10 @@ int64_t fp8_moe_route_workspace_size(int E);
 /*
  * fp8_moe_route -- routing and grouping of T tokens over E experts.
  *   x          BF16 tokens [T][ldx], D used (D % 32 == 0).
- *   centroids  FP32 [E][ldc]; bias FP32 [E] (selection only).
- *   logits     out FP32 [T][E]: l[t][e] = sum_k x[t][k] * c[e][k], formed in
+ *   centroids  FP32, k-major: [D][ldc], ldc >= E (expert e's centroid is
+ *              column e; a router weight stored once in the kernel's layout).
+ *   bias       FP32 [E] (selection only).
+ *   logits     out FP32 [T][E]: l[t][e] = sum_k x[t][k] * c[k][e], formed in
  *              FP32 with one fused multiply-add per term in increasing k (the
  *              decision below is taken from exactly these values).
  *   expert_idx out int32 [T][topk]: the topk experts with the largest
@@ -180,7 +182,7 @@ int64_t fp8_moe_route_workspace_size(int E);
  *              [T][topk] (row of token t's j-th listed expert).
  *   workspace  device, >= fp8_moe_route_workspace_size(E) bytes, 256-byte
  *              aligned, owned by the caller; contents on return unspecified.
- *   Requires 1 <= E <= 1024, 1 <= topk <= min(E, 16).  T == 0 writes zero
+ *   Requires 1 <= E <= 1024, E % 4 == 0, 1 <= topk <= min(E, 16).  T == 0 writes zero
  *   offsets.  Deterministic: no result depends on launch timing.
  */
 int fp8_moe_route(const void *x, int64_t T, int64_t D, int64_t ldx, const float *centroids, int64_t ldc,

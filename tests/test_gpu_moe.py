@@ -38,6 +38,11 @@ def _router_inputs(T, D, E, seed):
     return x, cent, bias
 
 
+def _cent_t(cent):
+    """Centroids in the kernel's k-major layout [D, E] (device)."""
+    return torch.from_numpy(np.ascontiguousarray(cent.T)).cuda()
+
+
 def _key_margin(logits, bias, k):
     """Gap between the k-th and (k+1)-th selection key per token (double)."""
     key = 1.0 / (1.0 + np.exp(-logits.astype(np.float64))) + bias.astype(np.float64)[None, :]
@@ -47,7 +52,7 @@ def _key_margin(logits, bias, k):
 
 def _check_route(fb, orc, x, cent, bias, k):
     T, E = x.shape[0], cent.shape[0]
-    r = fb.moe_route(dev(x), torch.from_numpy(cent).cuda(), torch.from_numpy(bias).cuda(), k)
+    r = fb.moe_route(dev(x), _cent_t(cent), torch.from_numpy(bias).cuda(), k)
     torch.cuda.synchronize()
     ol = orc.route_logits(x, cent)
     assert np.array_equal(r["logits"].cpu().numpy().view(np.uint32), ol.view(np.uint32)), "logits differ"
@@ -74,7 +79,7 @@ def test_route_small(fb, orc, T, D, E, k):
 def test_route_empty_batch(fb):
     E = 16
     r = fb.moe_route(torch.empty((0, 64), dtype=torch.bfloat16, device="cuda"),
-                     torch.zeros((E, 64), device="cuda"), torch.zeros(E, device="cuda"), 2)
+                     torch.zeros((64, E), device="cuda"), torch.zeros(E, device="cuda"), 2)
     torch.cuda.synchronize()
     assert r["offsets"].cpu().numpy().tolist() == [0] * (E + 1)
 
@@ -165,7 +170,7 @@ def test_chain_small(fb, orc):
     wd = synth.fill_bf16(synth.NORMAL, synth.key(79, 0), (E, D, Nh), 0.05)
     qwu, swu = _quant_experts(fb, wu)
     qwd, swd = _quant_experts(fb, wd)
-    r, h, sh, Y, out = _gpu_chain(fb, dev(x), torch.from_numpy(cent).cuda(), torch.from_numpy(bias).cuda(), k,
+    r, h, sh, Y, out = _gpu_chain(fb, dev(x), _cent_t(cent), torch.from_numpy(bias).cuda(), k,
                                   qwu, swu, qwd, swd)
     ol = orc.route_logits(x, cent)
     osel, ogate = orc.route_select(ol, bias, k)
@@ -199,7 +204,7 @@ def test_chain_full_layer_sampled_tokens(fb, orc):
         wd = dev(synth.moe_weights("down", e0, e0 + 16))
         fb.quant_128x128(wd.view(-1, Nh), q=qwd[e0:e0 + 16].view(-1, Nh), s=swd[e0:e0 + 16].view(-1, Nh // 128))
         del wu, wd
-    r, h, sh, Y, out = _gpu_chain(fb, dev(tok), torch.from_numpy(cent).cuda(), torch.from_numpy(bias).cuda(), k,
+    r, h, sh, Y, out = _gpu_chain(fb, dev(tok), _cent_t(cent), torch.from_numpy(bias).cuda(), k,
                                   qwu, swu, qwd, swd)
     ol = orc.route_logits(tok, cent)
     assert np.all(_key_margin(ol, bias, k) > 1e-12)
