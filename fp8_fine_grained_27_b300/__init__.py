@@ -15,6 +15,7 @@ from .binding import (  # noqa: F401
     lib,
     moe_combine,
     moe_route,
+    moe_route_noalloc,
     quant_1x128,
     quant_1x128_gather,
     quant_128x128,

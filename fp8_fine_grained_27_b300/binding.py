@@ -20,8 +20,8 @@ OK, EINVAL, EALIGN, EARCH, ECUDA, ETIMEOUT = 0, -1, -2, -3, -4, -5
 # every symbol include/fp8bs.h declares
 EXPORTS = (
     "fp8_quant_1x128", "fp8_quant_128x128", "fp8_quant_128x128_t", "fp8_gemm_blockscaled",
-    "fp8_grouped_gemm_moe", "fp8_moe_route_workspace_size", "fp8_moe_route", "fp8_quant_1x128_gather",
-    "fp8_grouped_gemm_moe_swiglu", "fp8_moe_combine", "fp8bs_e4m3_encode", "fp8bs_status_string",
+    "fp8_grouped_gemm_moe", "fp8_moe_route_workspace_size", "fp8_moe_route", "fp8_moe_route_noalloc",
+    "fp8_quant_1x128_gather", "fp8_grouped_gemm_moe_swiglu", "fp8_moe_combine", "fp8bs_e4m3_encode", "fp8bs_status_string",
     "fp8bs_get_device_error",
     "fp8bs_selftest_timeout", "fp8bs_selftest_division", "fp8bs_set_gemm_tile_n", "fp8bs_version",
 )
@@ -52,6 +52,7 @@ def lib() -> ctypes.CDLL:
         L.fp8_moe_route_workspace_size.argtypes = [i32]
         L.fp8_moe_route_workspace_size.restype = i64
         L.fp8_moe_route.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp, i64, vp]
+        L.fp8_moe_route_noalloc.argtypes = [vp, i64, i64, i64, vp, i64, vp, i32, i32, vp, vp, vp, vp, vp, vp, vp]
         L.fp8_quant_1x128_gather.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp]
         L.fp8_grouped_gemm_moe_swiglu.argtypes = [vp, i64, vp, i64, vp, vp, vp, i32, i64, vp, i64, vp, i64, i64,
                                                   i64, vp]
@@ -65,7 +66,7 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_set_gemm_tile_n.argtypes = [i32]
         L.fp8bs_version.restype = ctypes.c_char_p
         for name in ("fp8_quant_1x128", "fp8_quant_128x128", "fp8_quant_128x128_t", "fp8_gemm_blockscaled",
-                     "fp8_grouped_gemm_moe", "fp8_moe_route", "fp8_quant_1x128_gather",
+                     "fp8_grouped_gemm_moe", "fp8_moe_route", "fp8_moe_route_noalloc", "fp8_quant_1x128_gather",
                      "fp8_grouped_gemm_moe_swiglu", "fp8_moe_combine", "fp8bs_e4m3_encode", "fp8bs_get_device_error",
                      "fp8bs_selftest_timeout", "fp8bs_selftest_division", "fp8bs_set_gemm_tile_n"):
             getattr(L, name).restype = i32
@@ -204,6 +205,27 @@ def moe_route(x: torch.Tensor, centroids_t: torch.Tensor, bias: torch.Tensor, to
         _ptr(x), T, D, _ld(x), _ptr(centroids), _ld(centroids), _ptr(bias), E, topk,
         _ptr(o["logits"]), _ptr(o["expert_idx"]), _ptr(o["gate"]), _ptr(o["offsets"]),
         _ptr(o["token_of_row"]), _ptr(o["row_of"]), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return o
+
+
+def moe_route_noalloc(x: torch.Tensor, centroids_t: torch.Tensor, bias: torch.Tensor, topk: int, out=None,
+                      stream=None):
+    """moe_route without a workspace argument (the library's static device scratch)."""
+    T, D = x.shape
+    E = centroids_t.shape[1]
+    dev = x.device
+    o = out if out is not None else {
+        "logits": torch.empty((T, E), dtype=torch.float32, device=dev),
+        "expert_idx": torch.empty((T, topk), dtype=torch.int32, device=dev),
+        "gate": torch.empty((T, topk), dtype=torch.float32, device=dev),
+        "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+        "token_of_row": torch.empty(T * topk, dtype=torch.int32, device=dev),
+        "row_of": torch.empty((T, topk), dtype=torch.int32, device=dev),
+    }
+    _check("fp8_moe_route_noalloc", lib().fp8_moe_route_noalloc(
+        _ptr(x), T, D, _ld(x), _ptr(centroids_t), _ld(centroids_t), _ptr(bias), E, topk,
+        _ptr(o["logits"]), _ptr(o["expert_idx"]), _ptr(o["gate"]), _ptr(o["offsets"]),
+        _ptr(o["token_of_row"]), _ptr(o["row_of"]), _stream(stream)))
     return o
 
 

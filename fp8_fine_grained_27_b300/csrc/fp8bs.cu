@@ -15,6 +15,12 @@
 #include "ptx.cuh"
 #include "quant.cuh"
 
+// Library-owned scratch for fp8_moe_route_noalloc: the routing workspace of
+// the largest expert count (1024 experts x 4 bytes).  One buffer per device;
+// calls that use it on one device must be ordered (one stream, or events).
+static constexpr long long kRouteScratchBytes = 4096;
+static __device__ __align__(256) unsigned char g_route_scratch[kRouteScratchBytes];
+
 namespace fp8bs {
 
 // A barrier nothing completes, waited on with a short bound: exercises the
@@ -44,6 +50,7 @@ struct DeviceInfo {
     int quant_cols_ctas = 0;
     int quant_blockt_ctas = 0;
     unsigned gemm_attr_set = 0;  // bit per GEMM instance: shared-memory attribute applied
+    void *route_scratch = nullptr;  // device address of g_route_scratch
 };
 
 std::mutex g_mu;
@@ -547,6 +554,28 @@ int fp8_moe_route(const void *x, int64_t T, int64_t D, int64_t ldx, const float 
     }
     moe::route_group_kernel<<<E, 256, 0, st>>>(expert_idx, T, topk, E, counts, offsets, token_of_row, row_of);
     return launch_status();
+}
+
+int fp8_moe_route_noalloc(const void *x, int64_t T, int64_t D, int64_t ldx, const float *centroids, int64_t ldc,
+                          const float *bias, int E, int topk, float *logits, int32_t *expert_idx, float *gate,
+                          int32_t *offsets, int32_t *token_of_row, int32_t *row_of, void *stream)
+{
+    const int64_t need = fp8_moe_route_workspace_size(E);
+    if (need < 0 || need > kRouteScratchBytes)
+        return FP8BS_EINVAL;
+    DeviceInfo *d;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK)
+        return rc;
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!d->route_scratch && cudaGetSymbolAddress(&d->route_scratch, g_route_scratch) != cudaSuccess)
+            return FP8BS_ECUDA;
+        scratch = d->route_scratch;
+    }
+    return fp8_moe_route(x, T, D, ldx, centroids, ldc, bias, E, topk, logits, expert_idx, gate, offsets,
+                         token_of_row, row_of, scratch, kRouteScratchBytes, stream);
 }
 
 int fp8_moe_combine(const void *Y, int64_t ldy, int64_t R, const int32_t *row_of, const float *gate, int64_t T,

@@ -191,6 +191,19 @@ int fp8_moe_route(const void *x, int64_t T, int64_t D, int64_t ldx, const float 
                   int64_t workspace_bytes, void *stream);
 
 /*
+ * fp8_moe_route_noalloc -- fp8_moe_route without a caller workspace: the
+ * library uses its own static device scratch (4 KB per device, enough for
+ * E <= 1024) and allocates nothing.  The method as the pages describe it has
+ * no counterpart; this is a convenience of the interface.  Results are those
+ * of fp8_moe_route.  The scratch is one buffer per device, so calls on one
+ * device must be ordered (one stream, or events between streams).  An E
+ * whose workspace would not fit returns FP8BS_EINVAL before any launch.
+ */
+int fp8_moe_route_noalloc(const void *x, int64_t T, int64_t D, int64_t ldx, const float *centroids, int64_t ldc,
+                          const float *bias, int E, int topk, float *logits, int32_t *expert_idx, float *gate,
+                          int32_t *offsets, int32_t *token_of_row, int32_t *row_of, void *stream);
+
+/*
  * fp8_quant_1x128_gather -- fp8_quant_1x128 (along 0) of the rows
  * x[row_map[r]], r = 0 .. R-1: gathering and quantising in one pass (equal,
  * bit for bit, to quantising then gathering, since every scale belongs to
