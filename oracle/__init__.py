@@ -70,6 +70,13 @@ def lib():
         L.orc_e4m3_encode_buffer.restype = None
         L.orc_e4m3_encode_patterns.argtypes = [ctypes.c_uint64, i64, vp, i32]
         L.orc_e4m3_encode_patterns.restype = None
+        L.orc_pow2_exponent.argtypes = [ctypes.c_float]
+        L.orc_pow2_exponent.restype = i32
+        for fn in (L.orc_quant_1x128_rows_pow2, L.orc_quant_128x128_pow2):
+            fn.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, i32]
+            fn.restype = None
+        L.orc_gemm_exact_sum.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i32, i64, i64, vp, i64, vp, i32]
+        L.orc_gemm_exact_sum.restype = None
         L.orc_route_logits.argtypes = [vp, i64, i64, i64, vp, i64, i64, vp, i32]
         L.orc_route_logits.restype = None
         L.orc_route_select.argtypes = [vp, i64, i64, vp, i32, vp, vp]
@@ -301,4 +308,50 @@ def moe_combine(Y_bf16: np.ndarray, row_of: np.ndarray, gate: np.ndarray,
     N = Y.shape[1]
     out = np.empty((T, N), np.uint16)
     lib().orc_moe_combine(_p(Y), N, N, _p(row_of), _p(gate), T, k, _p(out), N, threads or nthreads())
+    return out
+
+
+# --- power-of-two (UE8M0) scales --------------------------------------------
+
+def pow2_exponent(amax: float) -> int:
+    """e of the tile scale 2^e: the smallest integer with amax <= 448 * 2^e (e >= -127; 0 for amax 0)."""
+    return int(lib().orc_pow2_exponent(float(amax)))
+
+
+def quant_1x128_rows_pow2(x_bf16: np.ndarray, threads: int | None = None):
+    """1x128 tiles with power-of-two scales: codes uint8 [M, K], scales f32 [K/128, M] (each 2^e)."""
+    x = _c(x_bf16, np.uint16)
+    M, K = x.shape
+    assert K % 128 == 0
+    q = np.empty((M, K), np.uint8)
+    s = np.empty((K // 128, M), np.float32)
+    lib().orc_quant_1x128_rows_pow2(_p(x), M, K, K, _p(q), K, _p(s), M, threads or nthreads())
+    return q, s
+
+
+def quant_128x128_pow2(w_bf16: np.ndarray, threads: int | None = None):
+    """128x128 blocks with power-of-two scales: codes uint8 [N, K], scales f32 [ceil(N/128), K/128]."""
+    w = _c(w_bf16, np.uint16)
+    N, K = w.shape
+    assert K % 128 == 0
+    q = np.empty((N, K), np.uint8)
+    s = np.empty(((N + 127) // 128, K // 128), np.float32)
+    lib().orc_quant_128x128_pow2(_p(w), N, K, K, _p(q), K, _p(s), K // 128, threads or nthreads())
+    return q, s
+
+
+def gemm_exact_sum(A, sa, B, sb, b_mode: int = 0, rows=None, threads: int | None = None) -> np.ndarray:
+    """fl32 of the double sum over all K of the scaled code products (layouts as gemm_blockscaled)."""
+    A = _c(A, np.uint8)
+    B = _c(B, np.uint8)
+    sa = _c(sa, np.float32)
+    sb = _c(sb, np.float32)
+    M, K = A.shape
+    N = B.shape[0]
+    if rows is None:
+        rows = np.arange(M, dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((rows.size, N), np.float32)
+    lib().orc_gemm_exact_sum(_p(A), K, _p(sa), M, _p(B), K, _p(sb), sb.shape[1], b_mode,
+                             N, K, _p(rows), rows.size, _p(out), threads or nthreads())
     return out

@@ -597,3 +597,109 @@ void orc_moe_combine(const uint16_t *Y, int64_t ldy, int64_t N, const int32_t *r
     cb_ctx c = {Y, ldy, N, row_of, gate, topk, out, ldo};
     parallel_for(T, nthreads, cb_token, &c);
 }
+
+/* ======================================================================== */
+/* Power-of-two (UE8M0) scales: the variant whose scales the tensor cores'  */
+/* block-scaled MMA can apply in hardware.  The scale of a tile is 2^e, e   */
+/* the smallest integer with amax <= 448 * 2^e (so no code saturates), kept */
+/* within UE8M0's range (e >= -127); an all-zero tile has e = 0.  Codes are */
+/* E4M3(x * 2^-e): the scaling itself is exact.                             */
+/* ======================================================================== */
+int orc_pow2_exponent(float amax)
+{
+    if (amax == 0.0f)
+        return 0;
+    int e = ilogb(amax) - 9; /* 448 * 2^e = 0.875 * 2^(ilogb+0) < amax: too small */
+    while ((double)amax > ldexp(448.0, e))
+        ++e;
+    return e < -127 ? -127 : e;
+}
+
+static uint8_t pow2_code(float x, int e) { return orc_e4m3_encode((float)ldexp((double)x, -e)); }
+
+static void q1p_row(void *p, int64_t m)
+{
+    q1_ctx *c = (q1_ctx *)p;
+    for (int64_t kb = 0; kb < c->K / 128; ++kb) {
+        const uint16_t *xt = c->x + m * c->ldx + kb * 128;
+        float amax = 0.0f;
+        for (int k = 0; k < 128; ++k) {
+            float a = fabsf(bf16_to_f32(xt[k]));
+            if (a > amax)
+                amax = a;
+        }
+        int e = orc_pow2_exponent(amax);
+        c->s[kb * c->lds + m] = (float)ldexp(1.0, e);
+        for (int k = 0; k < 128; ++k)
+            c->q[m * c->ldq + kb * 128 + k] = pow2_code(bf16_to_f32(xt[k]), e);
+    }
+}
+
+void orc_quant_1x128_rows_pow2(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                               uint8_t *q, int64_t ldq, float *s, int64_t lds, int nthreads)
+{
+    q1_ctx c = {x, M, K, ldx, q, ldq, s, lds};
+    parallel_for(M, nthreads, q1p_row, &c);
+}
+
+static void q3p_blockrow(void *p, int64_t nb)
+{
+    q3_ctx *c = (q3_ctx *)p;
+    int64_t r0 = nb * 128;
+    int64_t r1 = r0 + 128 < c->N ? r0 + 128 : c->N;
+    for (int64_t kb = 0; kb < c->K / 128; ++kb) {
+        float amax = 0.0f;
+        for (int64_t r = r0; r < r1; ++r)
+            for (int k = 0; k < 128; ++k) {
+                float a = fabsf(bf16_to_f32(c->w[r * c->ldw + kb * 128 + k]));
+                if (a > amax)
+                    amax = a;
+            }
+        int e = orc_pow2_exponent(amax);
+        c->s[nb * c->lds + kb] = (float)ldexp(1.0, e);
+        for (int64_t r = r0; r < r1; ++r)
+            for (int k = 0; k < 128; ++k)
+                c->q[r * c->ldq + kb * 128 + k] = pow2_code(bf16_to_f32(c->w[r * c->ldw + kb * 128 + k]), e);
+    }
+}
+
+void orc_quant_128x128_pow2(const uint16_t *w, int64_t N, int64_t K, int64_t ldw,
+                            uint8_t *q, int64_t ldq, float *s, int64_t lds, int nthreads)
+{
+    q3_ctx c = {w, N, K, ldw, q, ldq, s, lds};
+    parallel_for((N + 127) / 128, nthreads, q3p_blockrow, &c);
+}
+
+/* The product of the scaled codes summed in double over all of K, then     */
+/* rounded once to FP32: C[m][n] = fl32(sum_kb sa*sb * sum_k dec*dec).      */
+/* With power-of-two scales every term is exact in double, so this is the   */
+/* value a block-scaled tensor-core product approximates (it accumulates in */
+/* FP32 inside the MMA instead of promoting per chunk).                     */
+static void ge_row(void *p, int64_t r)
+{
+    g_ctx *c = (g_ctx *)p;
+    int64_t m = c->rows[r];
+    const uint8_t *a = c->A + m * c->lda;
+    for (int64_t n = 0; n < c->N; ++n) {
+        const uint8_t *b = c->B + n * c->ldb;
+        double acc = 0.0;
+        for (int64_t kb = 0; kb < c->K / 128; ++kb) {
+            double P = 0.0;
+            for (int k = 0; k < 128; ++k)
+                P += DEC[a[kb * 128 + k]] * DEC[b[kb * 128 + k]];
+            double s_a = c->sa[kb * c->ldsa + m];
+            double s_b = (c->b_mode == 0) ? c->sb[(n / 128) * c->ldsb + kb] : c->sb[kb * c->ldsb + n];
+            acc += s_a * s_b * P;
+        }
+        c->out[r * c->N + n] = (float)acc;
+    }
+}
+
+void orc_gemm_exact_sum(const uint8_t *A, int64_t lda, const float *sa, int64_t ldsa,
+                        const uint8_t *B, int64_t ldb, const float *sb, int64_t ldsb,
+                        int b_mode, int64_t N, int64_t K,
+                        const int64_t *rows, int64_t nrows, float *out, int nthreads)
+{
+    g_ctx c = {A, lda, sa, ldsa, B, ldb, sb, ldsb, b_mode, N, K, rows, out};
+    parallel_for(nrows, nthreads, ge_row, &c);
+}
