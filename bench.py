@@ -143,6 +143,13 @@ def workload_desc(name):
                 "quant": "A 1x128, [W_q; W_kv] 128x128", "out": "bf16"},
         "ffn": {"workload": "dense_ffn", "M": 16384, "K": 7168, "N": [18432],
                 "gemms": 1, "quant": "A 1x128, B 128x128", "out": "bf16"},
+        "ffn_ue8m0": {"workload": "dense_ffn_ue8m0_variant", "M": 16384, "K": 7168, "N": [18432], "gemms": 1,
+                      "quant": "A 1x128, B 128x128, power-of-two (UE8M0) scales",
+                      "gemm": "tcgen05 kind::mxf8f6f4 block-scaled MMA (no promotion pass)", "out": "bf16"},
+        "mla_ue8m0": {"workload": "mla_down_proj_ue8m0_variant", "M": 4096, "K": 7168, "N": [1536, 576],
+                      "gemms": "1 (stacked 2112-row weight)",
+                      "quant": "A 1x128, [W_q; W_kv] 128x128, power-of-two (UE8M0) scales",
+                      "gemm": "tcgen05 kind::mxf8f6f4 block-scaled MMA (no promotion pass)", "out": "bf16"},
         "wgrad": {"workload": "wgrad", "M": 2048, "K": 16384, "N": [7168],
                   "gemms": 1, "quant": "dY, X 1x128 along tokens (transposed)", "out": "fp32"},
         "dgrad": {"workload": "dgrad_ffn", "M": 16384, "K": 18432, "N": [7168], "gemms": 1,
@@ -174,7 +181,7 @@ def quant_bytes(name):
     """Algorithmic HBM bytes of the step's quantisation: BF16 read + code
     write + 4-byte scale per 128 elements (1x128) or per 128x128 block."""
     d = workload_desc(name)
-    if name in ("mla", "ffn", "tiny"):
+    if name in ("mla", "ffn", "tiny", "mla_ue8m0", "ffn_ue8m0"):
         ea = d["M"] * d["K"]
         ew = sum(d["N"]) * d["K"]
         return ea * (3 + 4 / 128) + ew * (3 + 4 / (128 * 128))
@@ -199,10 +206,10 @@ class Step:
         self.name, self.fb, self.torch = name, fb, torch
         dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16).cuda()  # noqa: E731
         self.kernels = []  # (label, kind) per launch, in order
-        if name in ("mla", "tiny"):
-            d = synth.mla(seed=seed) if name == "mla" else synth.tiny(seed=seed)
-            self.host = {"A": d["A"], "W": [np.concatenate([d["Wq"], d["Wkv"]])] if name == "mla" else [d["B"]]}
-        elif name == "ffn":
+        if name in ("mla", "tiny", "mla_ue8m0"):
+            d = synth.mla(seed=seed) if name != "tiny" else synth.tiny(seed=seed)
+            self.host = {"A": d["A"], "W": [np.concatenate([d["Wq"], d["Wkv"]])] if name != "tiny" else [d["B"]]}
+        elif name in ("ffn", "ffn_ue8m0"):
             d = synth.ffn(seed=seed)
             self.host = {"A": d["A"], "W": [d["B"]]}
         elif name == "wgrad":
@@ -219,7 +226,7 @@ class Step:
             offs, token_of_row = synth.moe_route(tok, seed=seed)
             self.host = {"A": np.ascontiguousarray(tok[token_of_row]), "offs": offs}
         self.d = {}
-        if name in ("mla", "tiny", "ffn"):
+        if name in ("mla", "tiny", "ffn", "mla_ue8m0", "ffn_ue8m0"):
             self.d["A"] = dev(self.host["A"])
             self.d["W"] = [dev(w) for w in self.host["W"]]
             M, K = self.host["A"].shape
@@ -301,6 +308,15 @@ class Step:
     def launches(self):
         """Return [(label, callable)] for one step."""
         fb, d = self.fb, self.d
+        if self.name in ("mla_ue8m0", "ffn_ue8m0"):
+            L = [("quant_1x128_ue8m0", lambda: fb.quant_1x128_ue8m0(d["A"], q=d["qa"], s=d["sa"]))]
+            for i in range(len(d["W"])):
+                L.append(("quant_128x128_ue8m0", lambda i=i: fb.quant_128x128_ue8m0(d["W"][i], q=d["qw"][i],
+                                                                                    s=d["sw"][i])))
+            for i in range(len(d["W"])):
+                L.append(("gemm_ue8m0", lambda i=i: fb.gemm_ue8m0(d["qa"], d["sa"], d["qw"][i], d["sw"][i],
+                                                                  C=d["C"][i])))
+            return L
         if self.name in ("mla", "tiny", "ffn"):
             L = [("quant_1x128", lambda: fb.quant_1x128(d["A"], q=d["qa"], s=d["sa"]))]
             for i in range(len(d["W"])):
@@ -335,7 +351,7 @@ class Step:
 
     def host_inputs(self):
         """(name, host array) of this step's BF16 inputs, for the end-to-end run."""
-        if self.name in ("mla", "tiny", "ffn"):
+        if self.name in ("mla", "tiny", "ffn", "mla_ue8m0", "ffn_ue8m0"):
             return [("A", self.host["A"])] + [(f"W{i}", w) for i, w in enumerate(self.host["W"])]
         if self.name == "wgrad":
             return [("dY", self.host["dY"]), ("X", self.host["X"])]
@@ -473,7 +489,7 @@ def run_e2e(args, step, torch, fb, launches, flops, world, dist):
     outs = step.d["C"]
     out_host = [torch.empty(c.shape, dtype=c.dtype).pin_memory() for c in outs]
     targets = {}
-    if step.name in ("mla", "tiny", "ffn"):
+    if step.name in ("mla", "tiny", "ffn", "mla_ue8m0", "ffn_ue8m0"):
         targets = {"A": step.d["A"], **{f"W{i}": w for i, w in enumerate(step.d["W"])}}
     elif step.name == "wgrad":
         targets = {"dY": step.d["dY"], "X": step.d["X"]}
@@ -529,6 +545,18 @@ def oracle_sample(workload, seed=0):
                 oracle.gemm_blockscaled(qa, sa, qb, sb, 0)
         flops = sum(2.0 * rows * W.shape[0] * W.shape[1] for W in Ws)
         return work, flops, f"{rows} of {d['A'].shape[0]} rows of A (quantise + both GEMMs) plus full weight quantisation"
+    if workload in ("mla_ue8m0", "ffn_ue8m0"):
+        d = synth.ffn(seed=seed, M=16, N=2048) if workload == "ffn_ue8m0" else synth.mla(seed=seed)
+        A = np.ascontiguousarray(d["A"][:16])
+        Ws = [d["B"]] if workload == "ffn_ue8m0" else [d["Wq"], d["Wkv"]]
+
+        def work():
+            qa, sa = oracle.quant_1x128_rows_pow2(A)
+            for W in Ws:
+                qb, sb = oracle.quant_128x128_pow2(W)
+                oracle.gemm_exact_sum(qa, sa, qb, sb, 0)
+        flops = sum(2.0 * 16 * W.shape[0] * W.shape[1] for W in Ws)
+        return work, flops, "16 rows of A (power-of-two quantisation + exact-sum GEMM) against the full weights"
     if workload == "ffn":
         d = synth.ffn(seed=seed, M=16, N=18432)
         A, B = d["A"], d["B"][:2048]
@@ -637,7 +665,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
-    ap.add_argument("--workload", default="mla", choices=["mla", "ffn", "wgrad", "dgrad", "moe", "moe_chain", "tiny"])
+    ap.add_argument("--workload", default="mla", choices=["mla", "ffn", "wgrad", "dgrad", "moe", "moe_chain", "tiny",
+                                                        "mla_ue8m0", "ffn_ue8m0"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
@@ -652,7 +681,7 @@ def main():
         run_reference(args, rank, world)
         return
     default_steps = {"mla": 10000, "tiny": 10000, "ffn": 200, "wgrad": 1000, "dgrad": 200, "moe": 300,
-                     "moe_chain": 200}[args.workload]
+                     "moe_chain": 200, "mla_ue8m0": 10000, "ffn_ue8m0": 200}[args.workload]
     args.steps = args.steps or default_steps
     args.warmup = max(3, args.warmup if args.warmup is not None else 20)
     run_ours(args, rank, world)

@@ -9,6 +9,7 @@ from .binding import (  # noqa: F401
     Fp8bsError,
     e4m3_encode,
     gemm_blockscaled,
+    gemm_ue8m0,
     get_device_error,
     grouped_gemm_moe,
     grouped_gemm_moe_swiglu,
@@ -18,7 +19,9 @@ from .binding import (  # noqa: F401
     moe_route_noalloc,
     quant_1x128,
     quant_1x128_gather,
+    quant_1x128_ue8m0,
     quant_128x128,
+    quant_128x128_ue8m0,
     quant_128x128_t,
     selftest_division,
     selftest_timeout,

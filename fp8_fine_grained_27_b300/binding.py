@@ -19,7 +19,8 @@ OK, EINVAL, EALIGN, EARCH, ECUDA, ETIMEOUT = 0, -1, -2, -3, -4, -5
 
 # every symbol include/fp8bs.h declares
 EXPORTS = (
-    "fp8_quant_1x128", "fp8_quant_128x128", "fp8_quant_128x128_t", "fp8_gemm_blockscaled",
+    "fp8_quant_1x128", "fp8_quant_128x128", "fp8_quant_128x128_t", "fp8_quant_1x128_ue8m0",
+    "fp8_quant_128x128_ue8m0", "fp8_gemm_ue8m0", "fp8_gemm_blockscaled",
     "fp8_grouped_gemm_moe", "fp8_moe_route_workspace_size", "fp8_moe_route", "fp8_moe_route_noalloc",
     "fp8_quant_1x128_gather", "fp8_grouped_gemm_moe_swiglu", "fp8_moe_combine", "fp8bs_e4m3_encode", "fp8bs_status_string",
     "fp8bs_get_device_error",
@@ -46,6 +47,9 @@ def lib() -> ctypes.CDLL:
         i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
         L.fp8_quant_1x128.argtypes = [vp, i64, i64, i64, i32, vp, i64, vp, i64, vp]
         L.fp8_quant_128x128.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp]
+        L.fp8_quant_1x128_ue8m0.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp]
+        L.fp8_quant_128x128_ue8m0.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp]
+        L.fp8_gemm_ue8m0.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i32, i64, i64, i64, vp]
         L.fp8_quant_128x128_t.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp]
         L.fp8_gemm_blockscaled.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i32, vp, i64, i32, i64, i64, i64, vp]
         L.fp8_grouped_gemm_moe.argtypes = [vp, i64, vp, i64, vp, vp, vp, i32, i64, vp, i64, i32, i64, i64, vp]
@@ -65,7 +69,8 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_selftest_division.argtypes = [vp, vp]
         L.fp8bs_set_gemm_tile_n.argtypes = [i32]
         L.fp8bs_version.restype = ctypes.c_char_p
-        for name in ("fp8_quant_1x128", "fp8_quant_128x128", "fp8_quant_128x128_t", "fp8_gemm_blockscaled",
+        for name in ("fp8_quant_1x128", "fp8_quant_128x128", "fp8_quant_128x128_t", "fp8_quant_1x128_ue8m0",
+                     "fp8_quant_128x128_ue8m0", "fp8_gemm_ue8m0", "fp8_gemm_blockscaled",
                      "fp8_grouped_gemm_moe", "fp8_moe_route", "fp8_moe_route_noalloc", "fp8_quant_1x128_gather",
                      "fp8_grouped_gemm_moe_swiglu", "fp8_moe_combine", "fp8bs_e4m3_encode", "fp8bs_get_device_error",
                      "fp8bs_selftest_timeout", "fp8bs_selftest_division", "fp8bs_set_gemm_tile_n"):
@@ -118,6 +123,26 @@ def quant_128x128(w: torch.Tensor, q=None, s=None, stream=None):
     return q, s
 
 
+def quant_1x128_ue8m0(x: torch.Tensor, q=None, s=None, stream=None):
+    """1x128 tiles with power-of-two scales: q [M, K], s [K/128, M] (FP32 powers of two)."""
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.uint8, device=x.device) if q is None else q
+    s = torch.empty((K // 128, M), dtype=torch.float32, device=x.device) if s is None else s
+    _check("fp8_quant_1x128_ue8m0", lib().fp8_quant_1x128_ue8m0(_ptr(x), M, K, _ld(x), _ptr(q), _ld(q), _ptr(s),
+                                                                _ld(s), _stream(stream)))
+    return q, s
+
+
+def quant_128x128_ue8m0(w: torch.Tensor, q=None, s=None, stream=None):
+    """128x128 blocks with power-of-two scales: q [N, K], s [ceil(N/128), K/128]."""
+    N, K = w.shape
+    q = torch.empty((N, K), dtype=torch.uint8, device=w.device) if q is None else q
+    s = torch.empty(((N + 127) // 128, K // 128), dtype=torch.float32, device=w.device) if s is None else s
+    _check("fp8_quant_128x128_ue8m0", lib().fp8_quant_128x128_ue8m0(_ptr(w), N, K, _ld(w), _ptr(q), _ld(q),
+                                                                    _ptr(s), _ld(s), _stream(stream)))
+    return q, s
+
+
 def quant_128x128_t(w: torch.Tensor, straight: bool = True, q=None, s=None, qt=None, st=None, stream=None):
     """128x128 block quantisation of BF16 w [N, K] with transposed outputs:
     qt [K, N] codes and st [K/128, ceil(N/128)] scales (the quantisation of w^T), plus, when
@@ -148,6 +173,19 @@ def gemm_blockscaled(A, sa, B, sb, b_scale_mode: int = 0, out_dtype=torch.bfloat
     _check("fp8_gemm_blockscaled", lib().fp8_gemm_blockscaled(
         _ptr(A), _ld(A), _ptr(sa), _ld(sa), _ptr(B), _ld(B), _ptr(sb), _ld(sb), b_scale_mode,
         _ptr(C), _ld(C), od, M, N, K, _stream(stream)))
+    return C
+
+
+def gemm_ue8m0(A, sa, B, sb, out_dtype=torch.bfloat16, C=None, stream=None):
+    """C = A * B^T with power-of-two scales applied by the tensor cores' block scaling."""
+    M, K = A.shape
+    N = B.shape[0]
+    if C is None:
+        C = torch.empty((M, N), dtype=out_dtype, device=A.device)
+    od = 0 if C.dtype == torch.bfloat16 else 1
+    _check("fp8_gemm_ue8m0", lib().fp8_gemm_ue8m0(
+        _ptr(A), _ld(A), _ptr(sa), _ld(sa), _ptr(B), _ld(B), _ptr(sb), _ld(sb), _ptr(C), _ld(C), od, M, N, K,
+        _stream(stream)))
     return C
 
 

@@ -12,6 +12,7 @@
 #include "../../include/fp8bs.h"
 #include "gemm.cuh"
 #include "moe.cuh"
+#include "mx.cuh"
 #include "ptx.cuh"
 #include "quant.cuh"
 
@@ -51,6 +52,7 @@ struct DeviceInfo {
     int quant_blockt_ctas = 0;
     unsigned gemm_attr_set = 0;  // bit per GEMM instance: shared-memory attribute applied
     void *route_scratch = nullptr;  // device address of g_route_scratch
+    unsigned mx_attr_set = 0;       // bit per block-scaled GEMM instance
 };
 
 std::mutex g_mu;
@@ -168,6 +170,25 @@ int launch_gemm_bn(int bn, int out_dtype, DeviceInfo *d, const CUtensorMap &tA, 
 
 std::atomic<int> g_tile_n{0};  // fp8bs_set_gemm_tile_n: 0 = automatic
 
+template <int BN, bool OUT_F32>
+int launch_mx(DeviceInfo *d, const CUtensorMap &tA, const CUtensorMap &tB, const mx::Params &p, int grid,
+              cudaStream_t st)
+{
+    using C = mx::Cfg<BN>;
+    auto kern = mx::mx_gemm_kernel<BN, OUT_F32>;
+    constexpr unsigned bit = 1u << ((BN == 256 ? 2 : 0) + (OUT_F32 ? 1 : 0));
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!(d->mx_attr_set & bit)) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::ALLOC) != cudaSuccess)
+                return FP8BS_ECUDA;
+            d->mx_attr_set |= bit;
+        }
+    }
+    kern<<<grid, mx::THREADS, C::ALLOC, st>>>(tA, tB, p);
+    return launch_status();
+}
+
 // Output tile width.  Per-row B scales (b_scale_mode 1) use 128.
 int pick_bn(int64_t M, int64_t N, int b_scale_mode, int num_sms)
 {
@@ -265,6 +286,54 @@ int fp8_quant_128x128(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t 
     const int64_t tiles = ((N + 127) / 128) * (K / 128);
     const int64_t grid = std::min<int64_t>(tiles, int64_t(d->num_sms) * d->quant_block_ctas);
     quant::quant_rows_kernel<true><<<static_cast<int>(grid), quant::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(w), N, K, ldw, q, ldq, s, lds);
+    return launch_status();
+}
+
+int fp8_quant_1x128_ue8m0(const void *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, int64_t ldq, float *s,
+                          int64_t lds, void *stream)
+{
+    if (M < 0 || K < 0)
+        return FP8BS_EINVAL;
+    if (M == 0 || K == 0)
+        return FP8BS_OK;
+    if (!x || !q || !s || ldx < K || K % 128 != 0 || ldq < K || lds < M)
+        return FP8BS_EINVAL;
+    if (M > (int64_t(1) << 31) || K > (int64_t(1) << 31))
+        return FP8BS_EINVAL;
+    if (!aligned16(x) || !aligned16(q) || (ldx * 2) % 16 != 0 || ldq % 16 != 0)
+        return FP8BS_EALIGN;
+    DeviceInfo *d;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK)
+        return rc;
+    const int64_t tiles = ((M + 127) / 128) * (K / 128);
+    const int64_t grid = std::min<int64_t>(tiles, int64_t(d->num_sms) * d->quant_rows_ctas);
+    quant::quant_rows_kernel<false, true><<<static_cast<int>(grid), quant::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t *>(x), M, K, ldx, q, ldq, s, lds);
+    return launch_status();
+}
+
+int fp8_quant_128x128_ue8m0(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq, float *s,
+                            int64_t lds, void *stream)
+{
+    if (N < 0 || K < 0)
+        return FP8BS_EINVAL;
+    if (N == 0 || K == 0)
+        return FP8BS_OK;
+    if (!w || !q || !s || ldw < K || ldq < K || K % 128 != 0 || lds < K / 128)
+        return FP8BS_EINVAL;
+    if (N > (int64_t(1) << 31) || K > (int64_t(1) << 31))
+        return FP8BS_EINVAL;
+    if (!aligned16(w) || !aligned16(q) || (ldw * 2) % 16 != 0 || ldq % 16 != 0)
+        return FP8BS_EALIGN;
+    DeviceInfo *d;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK)
+        return rc;
+    const int64_t tiles = ((N + 127) / 128) * (K / 128);
+    const int64_t grid = std::min<int64_t>(tiles, int64_t(d->num_sms) * d->quant_block_ctas);
+    quant::quant_rows_kernel<true, true><<<static_cast<int>(grid), quant::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t *>(w), N, K, ldw, q, ldq, s, lds);
     return launch_status();
 }
@@ -429,6 +498,47 @@ int fp8_grouped_gemm_moe(const uint8_t *A, int64_t lda, const float *sa, int64_t
     const int64_t max_tiles = ((M_total + 127) / 128 + G) * ((N + BN - 1) / BN);
     const int grid = static_cast<int>(std::min<int64_t>(max_tiles, d->num_sms));
     return launch_gemm_bn<0, true>(BN, out_dtype, d, tA, tB, tSB, p, grid, static_cast<cudaStream_t>(stream));
+}
+
+int fp8_gemm_ue8m0(const uint8_t *A, int64_t lda, const float *sa, int64_t ldsa, const uint8_t *B, int64_t ldb,
+                   const float *sb, int64_t ldsb, void *C, int64_t ldc, int out_dtype, int64_t M, int64_t N, int64_t K,
+                   void *stream)
+{
+    int rc = gemm_common_checks(A, lda, sa, ldsa, B, sb, C, ldc, out_dtype, M, N, K);
+    if (rc < 0)
+        return rc;
+    if (rc == 1)
+        return FP8BS_OK;
+    if (ldb < K || ldsb < K / 128)
+        return FP8BS_EINVAL;
+    if (ldb % 16 != 0)
+        return FP8BS_EALIGN;
+    DeviceInfo *d;
+    rc = current_device(&d);
+    if (rc != FP8BS_OK)
+        return rc;
+    mx::Params p;
+    p.sa = sa;
+    p.ldsa = ldsa;
+    p.sb = sb;
+    p.ldsb = ldsb;
+    p.C = C;
+    p.ldc = ldc;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    const int forced = g_tile_n.load(std::memory_order_relaxed);
+    const int BN = (forced == 192) ? 192 : 256;
+    CUtensorMap tA, tB;
+    if (make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, lda, 128, mx::BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        make_map(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, ldb, 128, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+        return FP8BS_EINVAL;
+    const int64_t tiles = ((M + mx::BM - 1) / mx::BM) * ((N + BN - 1) / BN);
+    const int grid = static_cast<int>(std::min<int64_t>(tiles, d->num_sms));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (BN == 256)
+        return out_dtype == 0 ? launch_mx<256, false>(d, tA, tB, p, grid, st) : launch_mx<256, true>(d, tA, tB, p, grid, st);
+    return out_dtype == 0 ? launch_mx<192, false>(d, tA, tB, p, grid, st) : launch_mx<192, true>(d, tA, tB, p, grid, st);
 }
 
 int fp8_grouped_gemm_moe_swiglu(const uint8_t *A, int64_t lda, const float *sa, int64_t ldsa, const uint8_t *B,

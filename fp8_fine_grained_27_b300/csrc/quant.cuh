@@ -50,6 +50,41 @@ __device__ __forceinline__ float tile_scale(float amax)
     return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
 }
 
+// Power-of-two (UE8M0) scale 2^e of a tile: e is the smallest integer with
+// amax <= 448 * 2^e = 1.75 * 2^(8+e).  With amax = 1.m * 2^E that is E - 8,
+// or E - 7 when 1.m > 1.75; kept >= -127 (UE8M0's range); 0 for amax 0.
+__device__ __forceinline__ float pow2_scale(float amax)
+{
+    if (amax == 0.0f)
+        return 1.0f;
+    const uint32_t b = __float_as_uint(amax);
+    int E;
+    uint32_t m;
+    if (b >> 23) {
+        E = static_cast<int>(b >> 23) - 127;
+        m = b & 0x7FFFFFu;
+    } else {  // subnormal: normalise
+        const int p = 31 - __clz(b);
+        E = p - 149;
+        m = (b << (23 - p)) & 0x7FFFFFu;
+    }
+    const int e = max(E - 8 + (m > 0x600000u ? 1 : 0), -127);
+    return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// 2^-e of a power-of-two scale 2^e (e in [-127, 127))
+__device__ __forceinline__ float pow2_inverse(float s)
+{
+    const uint32_t f = __float_as_uint(s) >> 23;
+    return f ? __uint_as_float((254u - f) << 23) : __uint_as_float(0x7F000000u);
+}
+
+// codes of BF16 pair word w scaled by a power of two (exact products)
+__device__ __forceinline__ uint32_t codes_pow2(uint32_t w, float inv)
+{
+    return e4m3x2(bf16lo(w) * inv, bf16hi(w) * inv);
+}
+
 // x / s for the two values of a BF16 pair, by Markstein's division
 // (P. Markstein, "Computation of elementary functions on the IBM RISC
 // System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with r = RN(1/s)
@@ -151,7 +186,7 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p)
 // [0, src_rows) reads as zeros.
 // Tile order: kb fastest, so neighbouring CTAs read neighbouring columns.
 // ---------------------------------------------------------------------------
-template <bool kBlock>
+template <bool kBlock, bool kPow2 = false>
 __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t *__restrict__ x, int64_t M,
                                                               int64_t K, int64_t ldx,
                                                               uint8_t *__restrict__ q, int64_t ldq,
@@ -195,7 +230,7 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t *__
                 uint32_t a = am[rr];
                 a = absmax2(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
                 a = absmax2(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-                sc[rr] = tile_scale(pair_max_to_f32(a));
+                sc[rr] = kPow2 ? pow2_scale(pair_max_to_f32(a)) : tile_scale(pair_max_to_f32(a));
             }
         } else {
             uint32_t a = absmax2(am[0], am[1]);
@@ -209,7 +244,7 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t *__
 #pragma unroll
             for (int w = 1; w < kThreads / 32; ++w)
                 b = absmax2(b, red[w]);
-            sc[0] = sc[1] = tile_scale(pair_max_to_f32(b));
+            sc[0] = sc[1] = kPow2 ? pow2_scale(pair_max_to_f32(b)) : tile_scale(pair_max_to_f32(b));
             __syncthreads();  // red[] is rewritten by the next tile
         }
 #pragma unroll
@@ -217,7 +252,15 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t *__
             const int64_t m = m0 + rw + 64 * rr;
             if (m < M) {
                 uint2 c[4];
-                if (markstein_ok(sc[rr])) {
+                if constexpr (kPow2) {
+                    const float inv = pow2_inverse(sc[rr]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint4 &x = v[rr][i];
+                        c[i].x = __byte_perm(codes_pow2(x.x, inv), codes_pow2(x.y, inv), 0x5410);
+                        c[i].y = __byte_perm(codes_pow2(x.z, inv), codes_pow2(x.w, inv), 0x5410);
+                    }
+                } else if (markstein_ok(sc[rr])) {
                     const Markstein2 d(sc[rr], sc[rr]);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {

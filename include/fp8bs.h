@@ -105,6 +105,39 @@ int fp8_quant_128x128_t(const void *w, int64_t N, int64_t K, int64_t ldw,
                         uint8_t *q, int64_t ldq, float *s, int64_t lds,
                         uint8_t *qt, int64_t ldqt, float *st, int64_t ldst, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Power-of-two (UE8M0) scale variant.  The scale of a tile is 2^e with e the
+ * smallest integer such that amax <= 448 * 2^e (so no code saturates), kept
+ * >= -127 (the UE8M0 range); an all-zero tile has scale 1.  Codes are
+ * E4M3_RNE(x * 2^-e), an exact scaling.  The scales are written as FP32
+ * powers of two, in the layouts of fp8_quant_1x128 (along 0) and
+ * fp8_quant_128x128, so both GEMM entry points take them; the UE8M0 byte
+ * is the FP32 exponent field.  The pages' method uses amax/448 scales; the
+ * power-of-two rule is the variant whose scales the tensor cores' block-
+ * scaled MMA applies in hardware (it changes the numerics: at most one
+ * binade of E4M3 range is given up per tile).
+ * ------------------------------------------------------------------------ */
+int fp8_quant_1x128_ue8m0(const void *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, int64_t ldq, float *s,
+                          int64_t lds, void *stream);
+int fp8_quant_128x128_ue8m0(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t *q, int64_t ldq, float *s,
+                            int64_t lds, void *stream);
+
+/*
+ * fp8_gemm_ue8m0 -- C = A * B^T for operands quantised with power-of-two
+ * scales (fp8_quant_1x128_ue8m0, fp8_quant_128x128_ue8m0), on the tensor
+ * cores' own block scaling (tcgen05 kind::mxf8f6f4, one UE8M0 scale per row
+ * per 32 K): the products are scaled inside the MMA and the whole K is
+ * accumulated in FP32 in tensor memory, with no promotion pass, so
+ *     C[m][n] ~= sum_kb sa[kb][m] * sb(n, kb) * sum_k dec(A) dec(B)
+ * up to the tensor core's FP32 accumulation.  Arguments and layouts as
+ * fp8_gemm_blockscaled with b_scale_mode 0; every scale must be a power of
+ * two within 2^-127 .. 2^127 (the _ue8m0 quantisers write nothing else; the
+ * kernel takes the FP32 exponent field as the UE8M0 byte).
+ */
+int fp8_gemm_ue8m0(const uint8_t *A, int64_t lda, const float *sa, int64_t ldsa, const uint8_t *B, int64_t ldb,
+                   const float *sb, int64_t ldsb, void *C, int64_t ldc, int out_dtype, int64_t M, int64_t N, int64_t K,
+                   void *stream);
+
 /*
  * fp8_gemm_blockscaled -- C = A * B^T from E4M3 codes with fine-grained
  * scales and FP32 promotion every 128 K (V3 report §6, §6.2).
@@ -265,12 +298,13 @@ int fp8bs_e4m3_encode(const float *x, uint8_t *q, int64_t n, void *stream);
 int fp8bs_selftest_division(unsigned long long *counts, void *stream);
 
 /*
- * fp8bs_set_gemm_tile_n -- output tile width (N per CTA tile) of both GEMM
+ * fp8bs_set_gemm_tile_n -- output tile width (N per CTA tile) of the GEMM
  * entry points for block-scaled B: 128, 192 or 256, or 0 to let the library
  * choose from the problem shape (the default).  Process-wide; results do not
  * depend on it (every output element is computed the same way), only speed.
  * Per-row B scales (b_scale_mode 1) come in widths 128 and 256 only; a
- * forced 192 leaves them on the automatic choice.
+ * forced 192 leaves them on the automatic choice.  fp8_gemm_ue8m0 uses 256
+ * unless 192 is forced.
  */
 int fp8bs_set_gemm_tile_n(int bn);
 
