@@ -41,7 +41,9 @@ FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1
 
 
 PROFILES = os.path.join(ROOT, "profiles")
-GEMM_PROFILE = {"mla": "gemm_kernel_mla_4096x2112x7168.md"}
+# workload -> (ncu summary under profiles/, sources whose hash it records)
+GEMM_PROFILE = {"mla": ("gemm_kernel_mla_4096x2112x7168.md", ["gemm.cuh", "ptx.cuh"]),
+                "mla_ue8m0": ("mx_gemm_kernel_mla_ue8m0.md", ["mx.cuh", "gemm.cuh", "ptx.cuh"])}
 
 
 def kernel_source_hash(files):
@@ -56,15 +58,16 @@ def kernel_source_hash(files):
 def profiled_traffic(workload):
     """DRAM bytes per GEMM launch from the committed ncu summary of this
     workload, or None if there is none or the kernel source changed since."""
-    name = GEMM_PROFILE.get(workload)
-    if not name:
+    entry = GEMM_PROFILE.get(workload)
+    if not entry:
         return None
+    name, sources = entry
     try:
         text = open(os.path.join(PROFILES, name)).read()
     except OSError:
         return None
     fields = dict(l.split(":", 1) for l in text.splitlines() if l.startswith(("kernel_source_sha256_16:", "traffic_bytes_per_launch:")))
-    if fields.get("kernel_source_sha256_16", "").split()[0:1] != [kernel_source_hash(["gemm.cuh", "ptx.cuh"])]:
+    if fields.get("kernel_source_sha256_16", "").split()[0:1] != [kernel_source_hash(sources)]:
         return None
     return int(fields["traffic_bytes_per_launch"].split()[0])
 
@@ -136,6 +139,11 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ workloads
+# tokens and experts of the moe_chain layer (--tokens / --experts; a smaller layer is for
+# profiling captures that must fit in a few GB)
+MOE_CHAIN = {"tokens": 4096, "experts": 256}
+
+
 def workload_desc(name):
     return {
         "mla": {"workload": "mla_down_proj", "M": 4096, "K": 7168, "N": [1536, 576],
@@ -154,8 +162,8 @@ def workload_desc(name):
                   "gemms": 1, "quant": "dY, X 1x128 along tokens (transposed)", "out": "fp32"},
         "dgrad": {"workload": "dgrad_ffn", "M": 16384, "K": 18432, "N": [7168], "gemms": 1,
                   "quant": "dY 1x128, W 128x128 written transposed (codes + scales)", "out": "bf16"},
-        "moe_chain": {"workload": "moe_layer_forward", "M": 32768, "K": [7168, 2048], "N": [4096, 7168],
-                      "tokens": 4096, "experts": 256, "topk": 8,
+        "moe_chain": {"workload": "moe_layer_forward", "M": 8 * MOE_CHAIN["tokens"], "K": [7168, 2048],
+                      "N": [4096, 7168], "tokens": MOE_CHAIN["tokens"], "experts": MOE_CHAIN["experts"], "topk": 8,
                       "gemms": "2 grouped (up 2x2048 with fused SwiGLU + 1x128 quantise; down 7168)",
                       "quant": "gathered token rows 1x128 (weights pre-quantised)",
                       "other": "routing (FP32 logits, top-8, grouping), combine", "out": "bf16"},
@@ -219,8 +227,8 @@ class Step:
             d = synth.dgrad(seed=seed)
             self.host = {"dY": d["dY"], "W": d["W"]}
         elif name == "moe_chain":
-            cent, bias = synth.moe_router(seed=seed)
-            self.host = {"X": synth.moe_tokens(seed=seed), "cent": cent, "bias": bias}
+            cent, bias = synth.moe_router(seed=seed, E=MOE_CHAIN["experts"])
+            self.host = {"X": synth.moe_tokens(seed=seed, T=MOE_CHAIN["tokens"]), "cent": cent, "bias": bias}
         elif name == "moe":
             tok = synth.moe_tokens(seed=seed)
             offs, token_of_row = synth.moe_route(tok, seed=seed)
@@ -256,7 +264,7 @@ class Step:
             self.d["C"] = [torch.empty((T, Ci), dtype=torch.bfloat16, device="cuda")]
         elif name == "moe_chain":
             T, D = self.host["X"].shape
-            E, k, Nh = 256, 8, 2048
+            E, k, Nh = MOE_CHAIN["experts"], 8, 2048
             R = T * k
             self.d["X"] = dev(self.host["X"])
             self.d["cent"] = torch.from_numpy(np.ascontiguousarray(self.host["cent"].T)).cuda()  # k-major
@@ -672,7 +680,12 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--flush-mb", type=int, default=256, help="L2 flush buffer (> 126 MB L2)")
+    ap.add_argument("--tokens", type=int, default=4096, help="moe_chain: tokens per step")
+    ap.add_argument("--experts", type=int, default=256, help="moe_chain: routed experts (a multiple of 16)")
     args = ap.parse_args()
+    if args.experts % 16 != 0 or not 16 <= args.experts <= 1024 or args.tokens < 1:
+        ap.error("--experts must be a multiple of 16 in 16..1024 and --tokens positive")
+    MOE_CHAIN.update(tokens=args.tokens, experts=args.experts)
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", args.gpus))
     if args.impl == "reference":
