@@ -317,18 +317,17 @@ class Step:
         """Return [(label, callable)] for one step."""
         fb, d = self.fb, self.d
         if self.name in ("mla_ue8m0", "ffn_ue8m0"):
-            L = [("quant_1x128_ue8m0", lambda: fb.quant_1x128_ue8m0(d["A"], q=d["qa"], s=d["sa"]))]
-            for i in range(len(d["W"])):
-                L.append(("quant_128x128_ue8m0", lambda i=i: fb.quant_128x128_ue8m0(d["W"][i], q=d["qw"][i],
-                                                                                    s=d["sw"][i])))
+            # one launch quantises the activation and the (stacked) weight
+            L = [("quant_act_weight_ue8m0", lambda: fb.quant_act_weight(d["A"], d["W"][0], ue8m0=True, qx=d["qa"],
+                                                                        sx=d["sa"], qw=d["qw"][0], sw=d["sw"][0]))]
             for i in range(len(d["W"])):
                 L.append(("gemm_ue8m0", lambda i=i: fb.gemm_ue8m0(d["qa"], d["sa"], d["qw"][i], d["sw"][i],
                                                                   C=d["C"][i])))
             return L
         if self.name in ("mla", "tiny", "ffn"):
-            L = [("quant_1x128", lambda: fb.quant_1x128(d["A"], q=d["qa"], s=d["sa"]))]
-            for i in range(len(d["W"])):
-                L.append(("quant_128x128", lambda i=i: fb.quant_128x128(d["W"][i], q=d["qw"][i], s=d["sw"][i])))
+            # one launch quantises the activation and the (stacked) weight
+            L = [("quant_act_weight", lambda: fb.quant_act_weight(d["A"], d["W"][0], qx=d["qa"], sx=d["sa"],
+                                                                  qw=d["qw"][0], sw=d["sw"][0]))]
             for i in range(len(d["W"])):
                 L.append(("gemm", lambda i=i: fb.gemm_blockscaled(d["qa"], d["sa"], d["qw"][i], d["sw"][i], 0,
                                                                   C=d["C"][i])))

@@ -21,6 +21,7 @@ from .binding import (  # noqa: F401
     quant_1x128_gather,
     quant_1x128_ue8m0,
     quant_128x128,
+    quant_act_weight,
     quant_128x128_ue8m0,
     quant_128x128_t,
     selftest_division,

@@ -20,7 +20,7 @@ OK, EINVAL, EALIGN, EARCH, ECUDA, ETIMEOUT = 0, -1, -2, -3, -4, -5
 # every symbol include/fp8bs.h declares
 EXPORTS = (
     "fp8_quant_1x128", "fp8_quant_128x128", "fp8_quant_128x128_t", "fp8_quant_1x128_ue8m0",
-    "fp8_quant_128x128_ue8m0", "fp8_gemm_ue8m0", "fp8_gemm_blockscaled",
+    "fp8_quant_128x128_ue8m0", "fp8_quant_act_weight", "fp8_gemm_ue8m0", "fp8_gemm_blockscaled",
     "fp8_grouped_gemm_moe", "fp8_moe_route_workspace_size", "fp8_moe_route", "fp8_moe_route_noalloc",
     "fp8_quant_1x128_gather", "fp8_grouped_gemm_moe_swiglu", "fp8_moe_combine", "fp8bs_e4m3_encode", "fp8bs_status_string",
     "fp8bs_get_device_error",
@@ -49,6 +49,8 @@ def lib() -> ctypes.CDLL:
         L.fp8_quant_128x128.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp]
         L.fp8_quant_1x128_ue8m0.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp]
         L.fp8_quant_128x128_ue8m0.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp]
+        L.fp8_quant_act_weight.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, i64, i64, vp, i64, vp, i64,
+                                           i32, vp]
         L.fp8_gemm_ue8m0.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i32, i64, i64, i64, vp]
         L.fp8_quant_128x128_t.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp]
         L.fp8_gemm_blockscaled.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i32, vp, i64, i32, i64, i64, i64, vp]
@@ -70,7 +72,7 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_set_gemm_tile_n.argtypes = [i32]
         L.fp8bs_version.restype = ctypes.c_char_p
         for name in ("fp8_quant_1x128", "fp8_quant_128x128", "fp8_quant_128x128_t", "fp8_quant_1x128_ue8m0",
-                     "fp8_quant_128x128_ue8m0", "fp8_gemm_ue8m0", "fp8_gemm_blockscaled",
+                     "fp8_quant_128x128_ue8m0", "fp8_quant_act_weight", "fp8_gemm_ue8m0", "fp8_gemm_blockscaled",
                      "fp8_grouped_gemm_moe", "fp8_moe_route", "fp8_moe_route_noalloc", "fp8_quant_1x128_gather",
                      "fp8_grouped_gemm_moe_swiglu", "fp8_moe_combine", "fp8bs_e4m3_encode", "fp8bs_get_device_error",
                      "fp8bs_selftest_timeout", "fp8bs_selftest_division", "fp8bs_set_gemm_tile_n"):
@@ -121,6 +123,22 @@ def quant_128x128(w: torch.Tensor, q=None, s=None, stream=None):
     _check("fp8_quant_128x128", lib().fp8_quant_128x128(_ptr(w), N, K, _ld(w), _ptr(q), _ld(q),
                                                         _ptr(s), _ld(s), _stream(stream)))
     return q, s
+
+
+def quant_act_weight(x: torch.Tensor, w: torch.Tensor, ue8m0: bool = False, qx=None, sx=None, qw=None, sw=None,
+                     stream=None):
+    """x [M, Kx] in 1x128 tiles and w [N, Kw] in 128x128 blocks, one launch.
+    Returns (qx [M, Kx], sx [Kx/128, M], qw [N, Kw], sw [ceil(N/128), Kw/128])."""
+    M, Kx = x.shape
+    N, Kw = w.shape
+    qx = torch.empty((M, Kx), dtype=torch.uint8, device=x.device) if qx is None else qx
+    sx = torch.empty((Kx // 128, M), dtype=torch.float32, device=x.device) if sx is None else sx
+    qw = torch.empty((N, Kw), dtype=torch.uint8, device=w.device) if qw is None else qw
+    sw = torch.empty(((N + 127) // 128, Kw // 128), dtype=torch.float32, device=w.device) if sw is None else sw
+    _check("fp8_quant_act_weight", lib().fp8_quant_act_weight(
+        _ptr(x), M, Kx, _ld(x), _ptr(qx), _ld(qx), _ptr(sx), _ld(sx), _ptr(w), N, Kw, _ld(w), _ptr(qw), _ld(qw),
+        _ptr(sw), _ld(sw), 1 if ue8m0 else 0, _stream(stream)))
+    return qx, sx, qw, sw
 
 
 def quant_1x128_ue8m0(x: torch.Tensor, q=None, s=None, stream=None):

@@ -50,6 +50,7 @@ struct DeviceInfo {
     int quant_block_ctas = 0;
     int quant_cols_ctas = 0;
     int quant_blockt_ctas = 0;
+    int quant_pair_ctas = 0;
     unsigned gemm_attr_set = 0;  // bit per GEMM instance: shared-memory attribute applied
     void *route_scratch = nullptr;  // device address of g_route_scratch
     unsigned mx_attr_set = 0;       // bit per block-scaled GEMM instance
@@ -85,6 +86,9 @@ int current_device(DeviceInfo **out)
                 cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.quant_block_ctas, quant::quant_rows_kernel<true>,
                                                               quant::kThreads, 0) != cudaSuccess)
                 return FP8BS_ECUDA;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.quant_pair_ctas, quant::quant_pair_kernel<false>,
+                                                              quant::kThreads, 0) != cudaSuccess)
+                return FP8BS_ECUDA;
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.quant_cols_ctas, quant::quant_t_kernel<false>,
                                                               quant::kThreads, 0) != cudaSuccess ||
                 cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.quant_blockt_ctas, quant::quant_t_kernel<true>,
@@ -109,6 +113,12 @@ int current_device(DeviceInfo **out)
 }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+quant::RowsArgs rows_args(const void *x, int64_t M, int64_t K, int64_t ldx, uint8_t *q, int64_t ldq, float *s,
+                          int64_t lds, const int32_t *row_map = nullptr, int64_t src_rows = 0)
+{
+    return quant::RowsArgs{static_cast<const uint16_t *>(x), M, K, ldx, q, ldq, s, lds, row_map, src_rows};
+}
 
 int launch_status()
 {
@@ -254,7 +264,7 @@ int fp8_quant_1x128(const void *x, int64_t M, int64_t K, int64_t ldx, int along,
         const int64_t tiles = ((M + 127) / 128) * (K / 128);
         const int64_t grid = std::min<int64_t>(tiles, int64_t(d->num_sms) * d->quant_rows_ctas);
         quant::quant_rows_kernel<false><<<static_cast<int>(grid), quant::kThreads, 0, st>>>(
-            static_cast<const uint16_t *>(x), M, K, ldx, q, ldq, s, lds);
+            rows_args(x, M, K, ldx, q, ldq, s, lds));
     } else {
         if (M % 128 != 0 || K % 8 != 0 || ldq < M || lds < K)
             return FP8BS_EINVAL;
@@ -286,7 +296,42 @@ int fp8_quant_128x128(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_t 
     const int64_t tiles = ((N + 127) / 128) * (K / 128);
     const int64_t grid = std::min<int64_t>(tiles, int64_t(d->num_sms) * d->quant_block_ctas);
     quant::quant_rows_kernel<true><<<static_cast<int>(grid), quant::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t *>(w), N, K, ldw, q, ldq, s, lds);
+        rows_args(w, N, K, ldw, q, ldq, s, lds));
+    return launch_status();
+}
+
+int fp8_quant_act_weight(const void *x, int64_t M, int64_t Kx, int64_t ldx, uint8_t *qx, int64_t ldqx, float *sx,
+                         int64_t ldsx, const void *w, int64_t N, int64_t Kw, int64_t ldw, uint8_t *qw, int64_t ldqw,
+                         float *sw, int64_t ldsw, int scale_rule, void *stream)
+{
+    if (M < 0 || Kx < 0 || N < 0 || Kw < 0 || (scale_rule != 0 && scale_rule != 1))
+        return FP8BS_EINVAL;
+    const bool do_x = M > 0 && Kx > 0, do_w = N > 0 && Kw > 0;
+    if (!do_x && !do_w)
+        return FP8BS_OK;
+    if (do_x && (!x || !qx || !sx || ldx < Kx || Kx % 128 != 0 || ldqx < Kx || ldsx < M))
+        return FP8BS_EINVAL;
+    if (do_w && (!w || !qw || !sw || ldw < Kw || Kw % 128 != 0 || ldqw < Kw || ldsw < Kw / 128))
+        return FP8BS_EINVAL;
+    if (M > (int64_t(1) << 31) || Kx > (int64_t(1) << 31) || N > (int64_t(1) << 31) || Kw > (int64_t(1) << 31))
+        return FP8BS_EINVAL;
+    if ((do_x && (!aligned16(x) || !aligned16(qx) || (ldx * 2) % 16 != 0 || ldqx % 16 != 0)) ||
+        (do_w && (!aligned16(w) || !aligned16(qw) || (ldw * 2) % 16 != 0 || ldqw % 16 != 0)))
+        return FP8BS_EALIGN;
+    DeviceInfo *d;
+    int rc = current_device(&d);
+    if (rc != FP8BS_OK)
+        return rc;
+    // an absent operand contributes no tiles
+    const quant::RowsArgs ax = rows_args(x, do_x ? M : 0, do_x ? Kx : 128, ldx, qx, ldqx, sx, ldsx);
+    const quant::RowsArgs aw = rows_args(w, do_w ? N : 0, do_w ? Kw : 128, ldw, qw, ldqw, sw, ldsw);
+    const int64_t tiles = quant::rows_tiles(ax) + quant::rows_tiles(aw);
+    const int64_t grid = std::min<int64_t>(tiles, int64_t(d->num_sms) * d->quant_pair_ctas);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (scale_rule == 0)
+        quant::quant_pair_kernel<false><<<static_cast<int>(grid), quant::kThreads, 0, st>>>(ax, aw);
+    else
+        quant::quant_pair_kernel<true><<<static_cast<int>(grid), quant::kThreads, 0, st>>>(ax, aw);
     return launch_status();
 }
 
@@ -310,7 +355,7 @@ int fp8_quant_1x128_ue8m0(const void *x, int64_t M, int64_t K, int64_t ldx, uint
     const int64_t tiles = ((M + 127) / 128) * (K / 128);
     const int64_t grid = std::min<int64_t>(tiles, int64_t(d->num_sms) * d->quant_rows_ctas);
     quant::quant_rows_kernel<false, true><<<static_cast<int>(grid), quant::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t *>(x), M, K, ldx, q, ldq, s, lds);
+        rows_args(x, M, K, ldx, q, ldq, s, lds));
     return launch_status();
 }
 
@@ -334,7 +379,7 @@ int fp8_quant_128x128_ue8m0(const void *w, int64_t N, int64_t K, int64_t ldw, ui
     const int64_t tiles = ((N + 127) / 128) * (K / 128);
     const int64_t grid = std::min<int64_t>(tiles, int64_t(d->num_sms) * d->quant_block_ctas);
     quant::quant_rows_kernel<true, true><<<static_cast<int>(grid), quant::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t *>(w), N, K, ldw, q, ldq, s, lds);
+        rows_args(w, N, K, ldw, q, ldq, s, lds));
     return launch_status();
 }
 
@@ -614,7 +659,7 @@ int fp8_quant_1x128_gather(const void *x, int64_t T, int64_t K, int64_t ldx, con
     const int64_t tiles = ((R + 127) / 128) * (K / 128);
     const int64_t grid = std::min<int64_t>(tiles, int64_t(d->num_sms) * d->quant_rows_ctas);
     quant::quant_rows_kernel<false><<<static_cast<int>(grid), quant::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t *>(x), R, K, ldx, q, ldq, s, lds, row_map, T);
+        rows_args(x, R, K, ldx, q, ldq, s, lds, row_map, T));
     return launch_status();
 }
 

@@ -186,23 +186,35 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p)
 // [0, src_rows) reads as zeros.
 // Tile order: kb fastest, so neighbouring CTAs read neighbouring columns.
 // ---------------------------------------------------------------------------
-template <bool kBlock, bool kPow2 = false>
-__global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t *__restrict__ x, int64_t M,
-                                                              int64_t K, int64_t ldx,
-                                                              uint8_t *__restrict__ q, int64_t ldq,
-                                                              float *__restrict__ s, int64_t lds,
-                                                              const int32_t *__restrict__ row_map = nullptr,
-                                                              int64_t src_rows = 0)
+struct RowsArgs {
+    const uint16_t *x;
+    int64_t M, K, ldx;
+    uint8_t *q;
+    int64_t ldq;
+    float *s;
+    int64_t lds;
+    const int32_t *row_map;  // 1x128 only, may be null (see above)
+    int64_t src_rows;
+};
+
+__host__ __device__ inline int64_t rows_tiles(const RowsArgs &a) { return ((a.M + 127) / 128) * (a.K / 128); }
+
+// one 128 x 128 tile (index `tile`, kb fastest) of the quantisation above
+template <bool kBlock, bool kPow2>
+__device__ __forceinline__ void rows_tile(const RowsArgs &a, int64_t tile, uint32_t *red)
 {
-    __shared__ uint32_t red[kThreads / 32];
+    const uint16_t *__restrict__ x = a.x;
+    const int64_t M = a.M, K = a.K, ldx = a.ldx, ldq = a.ldq, lds = a.lds;
+    uint8_t *__restrict__ q = a.q;
+    float *__restrict__ s = a.s;
+    const int32_t *__restrict__ row_map = a.row_map;
+    const int64_t src_rows = a.src_rows;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int j = lane & 3;                       // column-group phase within the row
     const int rw = (tid >> 5) * 8 + (lane >> 2);  // 0..63
     const int64_t nkb = K / 128;
-    const int64_t ntiles = ((M + 127) / 128) * nkb;
-
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    {
         const int64_t kb = tile % nkb;
         const int64_t m0 = (tile / nkb) * 128;
         uint4 v[2][4];
@@ -286,6 +298,31 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const uint16_t *__
         }
         if (kBlock && tid == 0)
             s[(m0 / 128) * lds + kb] = sc[0];
+    }
+}
+
+template <bool kBlock, bool kPow2 = false>
+__global__ void __launch_bounds__(kThreads) quant_rows_kernel(const RowsArgs a)
+{
+    __shared__ uint32_t red[kThreads / 32];
+    const int64_t ntiles = rows_tiles(a);
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x)
+        rows_tile<kBlock, kPow2>(a, tile, red);
+}
+
+// An activation (1x128 tiles) and a weight (128x128 blocks) in one launch:
+// the tiles of both form one persistent work list, so two small tensors
+// keep the whole GPU busy together instead of one after the other.
+template <bool kPow2>
+__global__ void __launch_bounds__(kThreads) quant_pair_kernel(const RowsArgs act, const RowsArgs wt)
+{
+    __shared__ uint32_t red[kThreads / 32];
+    const int64_t ta = rows_tiles(act), tw = rows_tiles(wt);
+    for (int64_t tile = blockIdx.x; tile < ta + tw; tile += gridDim.x) {
+        if (tile < ta)
+            rows_tile<false, kPow2>(act, tile, red);
+        else
+            rows_tile<true, kPow2>(wt, tile - ta, red);
     }
 }
 

@@ -85,6 +85,21 @@ int fp8_quant_128x128(const void *w, int64_t N, int64_t K, int64_t ldw,
                       uint8_t *q, int64_t ldq, float *s, int64_t lds, void *stream);
 
 /*
+ * fp8_quant_act_weight -- fp8_quant_1x128 (along 0) of an activation x and
+ * fp8_quant_128x128 of a weight w in one launch (the two operands of a
+ * Linear's forward GEMM, V3 report §6.1): the tiles of both tensors form one
+ * work list, so that two small tensors keep the GPU busy together.
+ *   x, M, Kx, ldx, qx, ldqx, sx, ldsx   as fp8_quant_1x128 (along 0);
+ *   w, N, Kw, ldw, qw, ldqw, sw, ldsw   as fp8_quant_128x128;
+ *   scale_rule 0: amax/448 scales; 1: power-of-two (UE8M0) scales, as the
+ *   _ue8m0 quantisers below.  Results are bit-identical to the separate
+ *   calls.  Either operand may be empty (M or Kx, N or Kw == 0).
+ */
+int fp8_quant_act_weight(const void *x, int64_t M, int64_t Kx, int64_t ldx, uint8_t *qx, int64_t ldqx, float *sx,
+                         int64_t ldsx, const void *w, int64_t N, int64_t Kw, int64_t ldw, uint8_t *qw, int64_t ldqw,
+                         float *sw, int64_t ldsw, int scale_rule, void *stream);
+
+/*
  * fp8_quant_128x128_t -- per-block 128x128 quantisation of a BF16 weight
  * matrix that also writes the codes and block scales transposed, for the
  * Dgrad GEMM (V3 report §6: Dgrad takes the FP8 weights; §6.1: 128x128

@@ -215,3 +215,25 @@ def test_strided_views(fb, orc):
     qr, sr = orc.quant_1x128_rows(np.ascontiguousarray(a[:, :384]))
     assert np.array_equal(q.cpu().numpy(), qr) and np.array_equal(s.cpu().numpy(), sr)
 
+
+
+@pytest.mark.parametrize("ue8m0", [False, True], ids=["amax448", "ue8m0"])
+def test_act_weight_in_one_launch(fb, orc, ue8m0):
+    """The fused launch gives the separate quantisers' codes and scales bit for bit."""
+    d = synth.mla()
+    A, W = d["A"], np.concatenate([d["Wq"], d["Wkv"]])
+    qx, sx, qw, sw = fb.quant_act_weight(dev(A), dev(W), ue8m0=ue8m0)
+    torch.cuda.synchronize()
+    if ue8m0:
+        rx, rsx = orc.quant_1x128_rows_pow2(A)
+        rw, rsw = orc.quant_128x128_pow2(W)
+    else:
+        rx, rsx = orc.quant_1x128_rows(A)
+        rw, rsw = orc.quant_128x128(W)
+    assert np.array_equal(qx.cpu().numpy(), rx) and np.array_equal(sx.cpu().numpy(), rsx)
+    assert np.array_equal(qw.cpu().numpy(), rw) and np.array_equal(sw.cpu().numpy(), rsw)
+    # an empty activation leaves only the weight's tiles
+    e = torch.empty((0, 7168), dtype=torch.bfloat16, device="cuda")
+    _, _, qw2, sw2 = fb.quant_act_weight(e, dev(W), ue8m0=ue8m0)
+    torch.cuda.synchronize()
+    assert np.array_equal(qw2.cpu().numpy(), rw) and np.array_equal(sw2.cpu().numpy(), rsw)
