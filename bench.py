@@ -10,9 +10,17 @@ One step = one pass of the whole hot path over one batch of the workload:
   ffn   A 16384x7168 (Student-t), B 18432x7168: quantise both, one GEMM.
   wgrad dY 16384x2048, X 16384x7168: token-wise 1x128 quantise (transposed
         codes), dW = dY^T X with FP32 output.
+  dgrad dY 16384x18432, W 18432x7168: dY 1x128 and W's transposed 128x128
+        quantisation, dX = dY W (BF16 out).
   moe   4096 tokens routed top-8 over 256 experts (32768 rows): quantise the
         grouped rows, up grouped GEMM (N=4096, K=7168) with pre-quantised
         expert weights.
+  moe_chain  the whole routed-expert layer: routing (FP32 logits, top-8,
+        grouping), gather-quantise, up GEMM with fused SwiGLU + quantise,
+        down GEMM, combine (--tokens, --experts size it).
+  mla_ue8m0, ffn_ue8m0  the mla / ffn steps in the power-of-two (UE8M0)
+        scale variant on the tensor cores' block-scaled MMA.
+In the mla/ffn steps one launch quantises both the activation and the weight.
 Inputs are seeded synthetic tensors (synth/), resident in HBM before timing.
 L2 is flushed (a 256 MB write by default) before every timed step, outside the step's
 CUDA events.  Prints one JSON line (rank 0).

@@ -1,12 +1,12 @@
 // quant.cuh -- BF16 -> E4M3 tile quantisers (V3 report §6.1: 1x128 tiles
 // for activations, 128x128 blocks for weights, scales computed online).
 //
-// Every kernel reads BF16 with 16-byte loads, takes the tile amax on the
-// sign-cleared BF16 bit patterns (for finite inputs their unsigned order is
-// the order of magnitudes, so the maximum is exact), forms the scale
+// Every kernel reads BF16 with 16-byte loads, takes the tile amax with the
+// BF16 magnitude maximum (exact for finite inputs), forms the scale
 // amax / 448 with an IEEE single-precision divide (1.0 for an all-zero tile)
 // and each code as E4M3_RNE_sat(x / scale), with the codes identical to those
-// of the IEEE single-precision quotient (see Quotient below).
+// of the IEEE single-precision quotient (see Markstein2 below).  The
+// power-of-two variant rounds the scale up to 2^e and scales exactly.
 // All grids are persistent: a CTA walks tiles with a stride of gridDim.x.
 #pragma once
 #include <cstdint>
