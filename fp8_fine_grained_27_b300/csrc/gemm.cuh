@@ -501,10 +501,19 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
 
                 auto fold = [&](int pc, const uint32_t(&cur)[32]) {
                     if constexpr (BMODE == 0) {
+                        // fmaf(sc, P, acc) two columns per instruction (each lane rounds
+                        // exactly as the scalar fmaf)
                         const float scp = (SWIGLU && pc >= 2) ? scu : sc;
+                        uint64_t sc2;
+                        asm("mov.b64 %0, {%1, %1};" : "=l"(sc2) : "f"(scp));
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            acc[pc * 32 + j] = fmaf(scp, __uint_as_float(cur[j]), acc[pc * 32 + j]);
+                        for (int j = 0; j < 32; j += 2) {
+                            uint64_t a2, p2;
+                            asm("mov.b64 %0, {%1, %2};" : "=l"(a2) : "f"(acc[pc * 32 + j]), "f"(acc[pc * 32 + j + 1]));
+                            asm("mov.b64 %0, {%1, %2};" : "=l"(p2) : "r"(cur[j]), "r"(cur[j + 1]));
+                            asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a2) : "l"(sc2), "l"(p2));
+                            asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[pc * 32 + j]), "=f"(acc[pc * 32 + j + 1]) : "l"(a2));
+                        }
                     } else {
                         uint64_t sa2;
                         asm("mov.b64 %0, {%1, %1};" : "=l"(sa2) : "f"(sa_v));
