@@ -74,3 +74,38 @@ def test_status_strings_and_argument_errors(libpath):
     # empty problems are a successful no-op
     assert L.fp8_gemm_blockscaled(None, 128, None, 4, None, 128, None, 1, 0, None, 8, 0,
                                   0, 8, 128, None) == b.OK
+
+
+def test_empty_problems_return_before_any_launch(libpath):
+    """Empty inputs are a successful no-op and argument errors are caught without a device:
+    these calls never reach the GPU."""
+    from fp8_fine_grained_27_b300 import binding as b
+    L = b.lib()
+    vp = ctypes.c_void_p
+    assert L.fp8_quant_1x128(None, 0, 128, 128, 0, None, 128, None, 1, None) == b.OK
+    assert L.fp8_quant_1x128(None, 4, 0, 128, 1, None, 128, None, 1, None) == b.OK
+    assert L.fp8_quant_128x128(None, 0, 128, 128, None, 128, None, 1, None) == b.OK
+    assert L.fp8_quant_1x128_ue8m0(None, 0, 128, 128, None, 128, None, 1, None) == b.OK
+    assert L.fp8_quant_128x128_ue8m0(None, 4, 0, 128, None, 128, None, 1, None) == b.OK
+    assert L.fp8_quant_act_weight(None, 0, 128, 128, None, 128, None, 1, None, 0, 128, 128, None, 128, None, 1,
+                                  0, None) == b.OK
+    assert L.fp8_quant_act_weight(None, 0, 128, 128, None, 128, None, 1, None, 0, 128, 128, None, 128, None, 1,
+                                  2, None) == b.EINVAL  # unknown scale rule
+    assert L.fp8_quant_1x128_gather(None, 10, 128, 128, None, 0, None, 128, None, 1, None) == b.OK
+    assert L.fp8_gemm_ue8m0(None, 128, None, 4, None, 128, None, 1, None, 8, 0, 0, 8, 128, None) == b.OK
+    assert L.fp8_grouped_gemm_moe_swiglu(vp(16), 128, vp(16), 4, vp(16), vp(16), vp(16), 1, 0, vp(16), 128,
+                                         vp(16), 4, 128, 128, None) == b.OK
+    assert L.fp8_grouped_gemm_moe_swiglu(vp(16), 128, vp(16), 4, vp(16), vp(16), vp(16), 1, 4, vp(16), 128,
+                                         vp(16), 4, 100, 128, None) == b.EINVAL  # Nh % 128
+    assert L.fp8_moe_combine(None, 8, 0, None, None, 0, 2, 8, None, 8, None) == b.OK
+    assert L.fp8_moe_combine(vp(16), 8, 4, vp(16), vp(16), 2, 0, 8, vp(16), 8, None) == b.EINVAL  # topk 0
+    # routing: expert count not a multiple of 4, top-k above the expert count, D not a multiple of 32
+    ws = vp(256)
+    assert L.fp8_moe_route(vp(16), 4, 64, 64, vp(16), 8, vp(16), 6, 2, vp(16), vp(16), vp(16), vp(16), vp(16),
+                           vp(16), ws, 256, None) == b.EINVAL
+    assert L.fp8_moe_route(vp(16), 4, 64, 64, vp(16), 8, vp(16), 8, 9, vp(16), vp(16), vp(16), vp(16), vp(16),
+                           vp(16), ws, 256, None) == b.EINVAL
+    assert L.fp8_moe_route(vp(16), 4, 48, 64, vp(16), 8, vp(16), 8, 2, vp(16), vp(16), vp(16), vp(16), vp(16),
+                           vp(16), ws, 256, None) == b.EINVAL
+    assert L.fp8_moe_route(vp(16), 4, 64, 64, vp(16), 8, vp(16), 8, 2, vp(16), vp(16), vp(16), vp(16), vp(16),
+                           vp(16), ws, 16, None) == b.EINVAL  # workspace too small
