@@ -22,8 +22,9 @@ One step = one pass of the whole hot path over one batch of the workload:
         scale variant on the tensor cores' block-scaled MMA.
 In the mla/ffn steps one launch quantises both the activation and the weight.
 Inputs are seeded synthetic tensors (synth/), resident in HBM before timing.
-L2 is flushed (a 256 MB write by default) before every timed step, outside the step's
-CUDA events.  Prints one JSON line (rank 0).
+L2 is flushed before every timed step, outside the step's CUDA events: a 256 MB
+write, then a 256 MB read that evicts the dirty lines the write left
+(--flush-mode write keeps only the write).  Prints one JSON line (rank 0).
 
 --impl reference times the CPU oracle (oracle/) on a bounded sample of the
 same workload instead: the method's plain restatement on the host cores.
@@ -408,10 +409,21 @@ def run_ours(args, rank, world):
     step = Step(args.workload, fb, torch, seed=rank)
     launches = step.launches()
     flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device="cuda")
+    # A write-only flush leaves L2 full of dirty lines, which the step's first
+    # kernel then has to write back to HBM on top of its own traffic; reading a
+    # second buffer of the same size afterwards evicts them (outside the timed
+    # region) and leaves only clean lines of no use to the step.
+    flush_rd = torch.ones(args.flush_mb << 18, dtype=torch.float32, device="cuda") if args.flush_mode == "write+read" else None
+
+    def flush_l2():
+        flush.zero_()
+        if flush_rd is not None:
+            flush_rd.sum()
+
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         for _, f in launches:
             f()
     torch.cuda.synchronize()
@@ -419,7 +431,14 @@ def run_ours(args, rank, world):
         raise RuntimeError("device error during warm-up")
 
     nk = len(launches)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    # The timed region: each step's launches go out back to back, as a caller
+    # issues them, with events only around the step.  A second pass over the
+    # same number of steps puts events between the launches, for the
+    # per-kernel split (an event between two launches keeps the GEMM's set-up
+    # from overlapping the quantiser before it, so that pass is not the step
+    # time).
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    evk = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
     time.sleep(0.3)
@@ -428,24 +447,32 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     t0 = time.time()
     for k in range(args.steps):
-        flush.zero_()
+        flush_l2()
         ev[k][0].record(stream)
-        for j, (_, f) in enumerate(launches):
+        for _, f in launches:
             f()
-            ev[k][j + 1].record(stream)
+        ev[k][1].record(stream)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     t1 = time.time()
-    clocks = sampler.stop(t0, t1)
+    for k in range(args.steps):
+        flush_l2()
+        evk[k][0].record(stream)
+        for j, (_, f) in enumerate(launches):
+            f()
+            evk[k][j + 1].record(stream)
+    torch.cuda.synchronize()
+    t2 = time.time()
+    clocks = sampler.stop(t0, t2)
     if fb.get_device_error() != 0:
         raise RuntimeError("device error during the timed region")
 
-    per_step = [ev[k][0].elapsed_time(ev[k][nk]) for k in range(args.steps)]
+    per_step = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)]
     per_kernel = {}
     for k in range(args.steps):
         for j, (label, _) in enumerate(launches):
-            per_kernel.setdefault(label, []).append(ev[k][j].elapsed_time(ev[k][j + 1]))
+            per_kernel.setdefault(label, []).append(evk[k][j].elapsed_time(evk[k][j + 1]))
     ms_step = max_over_ranks(float(np.mean(per_step)), dist, "cuda")
 
     flops = gemm_flops(args.workload)
@@ -456,9 +483,9 @@ def run_ours(args, rank, world):
     fp8_peak_sustained = 2.0 * peaks.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
     # GEMM launches of one step (there may be several): their summed mean duration
     g_idx = [j for j, (l, _) in enumerate(launches) if l.startswith("gemm")]
-    gemm_ms = float(np.mean([sum(ev[k][j].elapsed_time(ev[k][j + 1]) for j in g_idx) for k in range(args.steps)]))
+    gemm_ms = float(np.mean([sum(evk[k][j].elapsed_time(evk[k][j + 1]) for j in g_idx) for k in range(args.steps)]))
     q_idx = [j for j, (l, _) in enumerate(launches) if l.startswith("quant")]
-    quant_ms = float(np.mean([sum(ev[k][j].elapsed_time(ev[k][j + 1]) for j in q_idx) for k in range(args.steps)]))
+    quant_ms = float(np.mean([sum(evk[k][j].elapsed_time(evk[k][j + 1]) for j in q_idx) for k in range(args.steps)]))
     achieved = flops / (gemm_ms * 1e-3) / 1e12
     quant_gbs = qbytes / (quant_ms * 1e-3) / 1e9
 
@@ -474,7 +501,7 @@ def run_ours(args, rank, world):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> fp32 accumulate",
         "data": "synthetic (seeded; shapes of the DeepSeek-V3 pages)",
-        "config": {**workload_desc(args.workload), "l2": f"flushed ({args.flush_mb} MB write) before every step",
+        "config": {**workload_desc(args.workload), "l2": f"flushed ({args.flush_mb} MB {args.flush_mode}) before every step",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(fp8_peak, 1),
                      "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
@@ -489,6 +516,7 @@ def run_ours(args, rank, world):
                   "frac": round(quant_gbs / peaks["hbm_gbs"], 4), "kernel_ms": round(quant_ms, 5),
                   "bytes_per_step": int(qbytes)},
         "per_kernel_ms": {l: round(float(np.mean(v)), 5) for l, v in per_kernel.items()},
+        "per_kernel_note": "second pass of the same steps with an event between launches",
         "e2e": e2e,
         "gpu_launches": sum(KERNELS_PER_CALL.get(l, 1) for l, _ in launches) * args.steps,
         "clocks": clocks,
@@ -521,24 +549,39 @@ def run_e2e(args, step, torch, fb, launches, flops, world, dist):
     h2d = sum(p.numel() * p.element_size() for _, p in pinned)
     d2h = sum(o.numel() * o.element_size() for o in out_host)
     n = max(3, min(args.e2e_steps, args.steps))
-    for _ in range(2):
+    # The read-back of step i runs on a side stream while step i+1's inputs
+    # go up on the launch stream (the link is full duplex); step i+1's
+    # launches wait for that read-back before they overwrite the outputs.
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+
+    def one_step(read_back_done):
         for name, p in pinned:
             targets[name].view(torch.int16).copy_(p.view(torch.int16), non_blocking=True)
+        if read_back_done is not None:
+            main.wait_event(read_back_done)
         for _, f in launches:
             f()
-        for o, h in zip(outs, out_host):
-            h.copy_(o, non_blocking=True)
+        computed = torch.cuda.Event()
+        computed.record(main)
+        side.wait_event(computed)
+        with torch.cuda.stream(side):
+            for o, h in zip(outs, out_host):
+                h.copy_(o, non_blocking=True)
+        done = torch.cuda.Event()
+        done.record(side)
+        return done
+
+    done = None
+    for _ in range(2):
+        done = one_step(done)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     t0 = time.perf_counter()
+    done = None
     for _ in range(n):
-        for name, p in pinned:
-            targets[name].view(torch.int16).copy_(p.view(torch.int16), non_blocking=True)
-        for _, f in launches:
-            f()
-        for o, h in zip(outs, out_host):
-            h.copy_(o, non_blocking=True)
+        done = one_step(done)
     torch.cuda.synchronize()
     dt = max_over_ranks((time.perf_counter() - t0) / n, dist, "cuda")
     return {"value": round(job_throughput(flops, dt, world) / 1e12, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
@@ -691,6 +734,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--flush-mb", type=int, default=256, help="L2 flush buffer (> 126 MB L2)")
+    ap.add_argument("--flush-mode", choices=("write", "write+read"), default="write+read",
+                    help="L2 flush: a write, or a write followed by a read of a second buffer")
     ap.add_argument("--tokens", type=int, default=4096, help="moe_chain: tokens per step")
     ap.add_argument("--experts", type=int, default=256, help="moe_chain: routed experts (a multiple of 16)")
     args = ap.parse_args()

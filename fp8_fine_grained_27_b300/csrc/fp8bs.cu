@@ -8,6 +8,7 @@
 #include <cstring>
 #include <atomic>
 #include <mutex>
+#include <utility>
 
 #include "../../include/fp8bs.h"
 #include "gemm.cuh"
@@ -141,6 +142,30 @@ int make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t 
 }
 
 // ------------------------------------------------------------------ GEMM
+// The GEMM kernels are launched with programmatic stream serialisation: when
+// the kernel before them is a quantiser (which signals early), their
+// prologue (barriers, TMEM, descriptor prefetch) runs on SMs the quantiser has
+// already left, and they wait on the device for its results.
+template <typename... KArgs, typename... Args>
+int launch_programmatic(void (*kern)(KArgs...), int grid, int threads, int smem, cudaStream_t st, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...) != cudaSuccess) {
+        cudaGetLastError();  // clear it, as launch_status() does
+        return FP8BS_ECUDA;
+    }
+    return launch_status();
+}
+
 template <int BN, int BMODE, bool OUT_F32, bool GROUPED, bool SWIGLU = false>
 int launch_gemm(DeviceInfo *d, const CUtensorMap &tA, const CUtensorMap &tB, const CUtensorMap &tSB,
                 const gemm::Params &p, int grid, cudaStream_t st)
@@ -158,8 +183,7 @@ int launch_gemm(DeviceInfo *d, const CUtensorMap &tA, const CUtensorMap &tB, con
             d->gemm_attr_set |= (1u << inst_bit);
         }
     }
-    kern<<<grid, C::THREADS, C::ALLOC, st>>>(tA, tB, tSB, p);
-    return launch_status();
+    return launch_programmatic(kern, grid, C::THREADS, C::ALLOC, st, tA, tB, tSB, p);
 }
 
 template <int BMODE, bool GROUPED>
@@ -195,8 +219,7 @@ int launch_mx(DeviceInfo *d, const CUtensorMap &tA, const CUtensorMap &tB, const
             d->mx_attr_set |= bit;
         }
     }
-    kern<<<grid, mx::THREADS, C::ALLOC, st>>>(tA, tB, p);
-    return launch_status();
+    return launch_programmatic(kern, grid, mx::THREADS, C::ALLOC, st, tA, tB, p);
 }
 
 // Output tile width.  Per-row B scales (b_scale_mode 1) use 128.

@@ -337,6 +337,8 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
         tmem_alloc(smem_addr(tmem_slot), L::TMEM_COLS);
         tmem_relinquish();
     }
+    // the set-up above overlaps the end of the kernel that produced the inputs
+    grid_dependency_wait();
     if constexpr (GROUPED) {
         if (warp >= kFirstPromoWarp)
             build_tile_start<L::NPW>(p, tile_start, threadIdx.x - kFirstPromoWarp * 32);

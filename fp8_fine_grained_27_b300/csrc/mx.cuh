@@ -167,6 +167,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_alloc(smem_addr(tmem_slot), 512);
         tmem_relinquish();
     }
+    // the set-up above overlaps the end of the kernel that produced the inputs
+    grid_dependency_wait();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

@@ -92,6 +92,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int cod
     }
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may be scheduled while the kernel before it in the stream is
+// still running: it must not read that kernel's results (or write what that
+// kernel reads) before grid_dependency_wait(), which returns once the earlier
+// grid has completed and its memory is visible.  The earlier kernel calls
+// grid_launch_dependents() to let the next one be scheduled before it ends.
+// Without a programmatic launch both are no-ops.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Re-balance registers between warpgroups (the four warps of a warpgroup
 // execute these together).
 template <int N>

@@ -305,6 +305,7 @@ template <bool kBlock, bool kPow2 = false>
 __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const RowsArgs a)
 {
     __shared__ uint32_t red[kThreads / 32];
+    grid_launch_dependents();  // a GEMM launched next may set up meanwhile
     const int64_t ntiles = rows_tiles(a);
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x)
         rows_tile<kBlock, kPow2>(a, tile, red);
@@ -317,6 +318,7 @@ template <bool kPow2>
 __global__ void __launch_bounds__(kThreads) quant_pair_kernel(const RowsArgs act, const RowsArgs wt)
 {
     __shared__ uint32_t red[kThreads / 32];
+    grid_launch_dependents();  // a GEMM launched next may set up meanwhile
     const int64_t ta = rows_tiles(act), tw = rows_tiles(wt);
     for (int64_t tile = blockIdx.x; tile < ta + tw; tile += gridDim.x) {
         if (tile < ta)
@@ -367,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, 4) quant_t_kernel(const uint16_t *__
 {
     __shared__ __align__(16) uint32_t qs[128 * 32];
     __shared__ __align__(16) uint4 red[kThreads / 32][16];
+    grid_launch_dependents();  // a GEMM launched next may set up meanwhile
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;

@@ -259,3 +259,52 @@ def test_mla_stacked_weight_equals_separate(fb, orc):
     oqw, osw = orc.quant_128x128(np.concatenate([d["Wq"], d["Wkv"]]))
     ref = orc.bf16_round(orc.gemm_blockscaled(oqa, osa, oqw, osw, 0, rows=rows))
     assert_gemm_close(host_bits(C[torch.from_numpy(rows).cuda()]), ref, "mla stacked")
+
+
+@pytest.mark.parametrize("ue8m0", [False, True], ids=["fp32_scales", "ue8m0"])
+def test_quantiser_then_gemm_back_to_back(fb, orc, ue8m0):
+    """The GEMMs are launched so that their set-up overlaps the quantiser before
+    them, and wait on the device for its codes.  Quantiser -> GEMM pairs issued
+    back to back into shared code buffers, on inputs that change every
+    iteration, give bit for bit the outputs of the same pairs run with a full
+    synchronisation between the two launches; the first is also checked against
+    the oracle."""
+    d = synth.mla()
+    A0 = dev(d["A"])
+    W = dev(np.concatenate([d["Wq"], d["Wkv"]]))
+    n = 6
+    A = [torch.roll(A0, shifts=37 * i, dims=0) for i in range(n)]
+    qa = torch.empty((4096, 7168), dtype=torch.uint8, device="cuda")
+    qw = torch.empty((2112, 7168), dtype=torch.uint8, device="cuda")
+    sa = torch.empty((56, 4096), dtype=torch.float32, device="cuda")
+    sw = torch.empty((17, 56), dtype=torch.float32, device="cuda")
+    gemm = fb.gemm_ue8m0 if ue8m0 else (lambda a, s, b, t, C: fb.gemm_blockscaled(a, s, b, t, 0, C=C))
+
+    def pair(i, C, sync):
+        fb.quant_act_weight(A[i], W, ue8m0=ue8m0, qx=qa, sx=sa, qw=qw, sw=sw)
+        if sync:
+            torch.cuda.synchronize()
+        gemm(qa, sa, qw, sw, C=C)
+
+    got = [torch.empty((4096, 2112), dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+    for i in range(n):
+        pair(i, got[i], sync=False)
+    torch.cuda.synchronize()
+    assert fb.get_device_error() == 0
+    for i in range(n):
+        ref = torch.empty_like(got[i])
+        pair(i, ref, sync=True)
+        torch.cuda.synchronize()
+        assert torch.equal(got[i], ref), f"iteration {i} differs from the synchronised run"
+    assert not torch.equal(got[0], got[1])
+    rows = sample_rows(4096, 32, seed=9, must=(0, 4095))
+    Wh = np.concatenate([d["Wq"], d["Wkv"]])
+    if ue8m0:
+        oqa, osa = orc.quant_1x128_rows_pow2(d["A"])
+        oqw, osw = orc.quant_128x128_pow2(Wh)
+        ref = orc.gemm_exact_sum(oqa, osa, oqw, osw, 0, rows=rows)
+    else:
+        oqa, osa = orc.quant_1x128_rows(d["A"])
+        oqw, osw = orc.quant_128x128(Wh)
+        ref = orc.gemm_blockscaled(oqa, osa, oqw, osw, 0, rows=rows)
+    assert_gemm_close(host_bits(got[0][torch.from_numpy(rows).cuda()]), orc.bf16_round(ref), "back to back")
