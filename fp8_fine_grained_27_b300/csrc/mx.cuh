@@ -298,52 +298,76 @@ __global__ void __launch_bounds__(THREADS, 1)
                 break;
             tc_fence_after();
             const int grow0 = tl.m0 + q * 32;
-            constexpr int COLS_PER_ROUND = OUT_F32 ? 16 : 32;
-            constexpr int ELEMS_PER_CHUNK = OUT_F32 ? 4 : 8;
-            constexpr int PIECES = BN / 64;
-#pragma unroll 1
-            for (int pi = 0; pi < PIECES; ++pi) {
-                const int pc = half * PIECES + pi;
-                uint32_t r[32];
-                tmem_ld32(tmem_base + lanes + b * BN + pc * 32, r);
-                tmem_ld_wait();
-                if (pi == PIECES - 1) {  // this group's share of the accumulator has been read
-                    tc_fence_before();
-                    mbar_arrive(bar_tempty + 8 * b);
+            constexpr int PIECES = BN / 64;  // 32-column pieces of this warp's half
+            // one round: 32 rows x 64 bytes staged through the warp's 2 KB
+            // (16-byte chunks XOR-swizzled by row pair: conflict-free both
+            // ways), then 16-byte stores with row / column masks
+            auto stage = [&](const uint32_t *w) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4 *>(epi + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)) =
+                        make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+            };
+            auto flush = [&](int n0) {
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int idx = lane + 32 * i;
+                    const int rr = idx >> 2, j = idx & 3;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(epi + rr * 64 + ((j ^ ((rr >> 1) & 3)) * 16));
+                    const int m = grow0 + rr;
+                    const int n = n0 + j * (OUT_F32 ? 4 : 8);
+                    if (m < p.M && n < p.N) {
+                        const int64_t off = static_cast<int64_t>(m) * p.ldc + n;
+                        if constexpr (OUT_F32)
+                            *reinterpret_cast<uint4 *>(reinterpret_cast<float *>(p.C) + off) = v;
+                        else
+                            *reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.C) + off) = v;
+                    }
                 }
+                __syncwarp();
+            };
+            if constexpr (!OUT_F32) {
+                // Read the whole share as packed BF16 (16 registers a piece;
+                // the first piece goes straight to the staging buffer), free
+                // the accumulator, then store: the next tile's MMAs run while
+                // the stores drain.
+                uint32_t packed[PIECES * 16];
 #pragma unroll
-                for (int g = 0; g < 32 / COLS_PER_ROUND; ++g) {
+                for (int pi = 0; pi < PIECES; ++pi) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem_base + lanes + b * BN + (half * PIECES + pi) * 32, r);
+                    gemm::tmem_ld_wait_regs(r);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint32_t *a = &r[g * COLS_PER_ROUND + j * ELEMS_PER_CHUNK];
-                        uint4 v;
-                        if constexpr (OUT_F32) {
-                            v = make_uint4(a[0], a[1], a[2], a[3]);
-                        } else {
-                            v = make_uint4(gemm::pack_bf16x2(__uint_as_float(a[0]), __uint_as_float(a[1])),
-                                           gemm::pack_bf16x2(__uint_as_float(a[2]), __uint_as_float(a[3])),
-                                           gemm::pack_bf16x2(__uint_as_float(a[4]), __uint_as_float(a[5])),
-                                           gemm::pack_bf16x2(__uint_as_float(a[6]), __uint_as_float(a[7])));
-                        }
-                        *reinterpret_cast<uint4 *>(epi + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)) = v;
+                    for (int i = 0; i < 16; ++i)
+                        packed[pi * 16 + i] = gemm::pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                    if (pi == 0)
+                        stage(&packed[0]);
+                }
+                tc_fence_before();
+                mbar_arrive(bar_tempty + 8 * b);
+                flush(tl.n0 + half * PIECES * 32);
+#pragma unroll
+                for (int pi = 1; pi < PIECES; ++pi) {
+                    stage(&packed[pi * 16]);
+                    flush(tl.n0 + (half * PIECES + pi) * 32);
+                }
+            } else {
+                // FP32: a piece at a time (the share does not fit in registers)
+#pragma unroll 1
+                for (int pi = 0; pi < PIECES; ++pi) {
+                    const int pc = half * PIECES + pi;
+                    uint32_t r[32];
+                    tmem_ld32(tmem_base + lanes + b * BN + pc * 32, r);
+                    gemm::tmem_ld_wait_regs(r);
+                    if (pi == PIECES - 1) {  // this group's share of the accumulator has been read
+                        tc_fence_before();
+                        mbar_arrive(bar_tempty + 8 * b);
                     }
-                    __syncwarp();
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int idx = lane + 32 * i;
-                        const int rr = idx >> 2, j = idx & 3;
-                        const uint4 v = *reinterpret_cast<const uint4 *>(epi + rr * 64 + ((j ^ ((rr >> 1) & 3)) * 16));
-                        const int m = grow0 + rr;
-                        const int n = tl.n0 + pc * 32 + g * COLS_PER_ROUND + j * ELEMS_PER_CHUNK;
-                        if (m < p.M && n < p.N) {
-                            const int64_t off = static_cast<int64_t>(m) * p.ldc + n;
-                            if constexpr (OUT_F32)
-                                *reinterpret_cast<uint4 *>(reinterpret_cast<float *>(p.C) + off) = v;
-                            else
-                                *reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.C) + off) = v;
-                        }
-                    }
-                    __syncwarp();
+                    stage(&r[0]);
+                    flush(tl.n0 + pc * 32);
+                    stage(&r[16]);
+                    flush(tl.n0 + pc * 32 + 16);
                 }
             }
         }
