@@ -545,6 +545,21 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                     release();
                     fold(0, ra);
                     fold(1, rb);
+                } else if constexpr (BMODE == 1) {
+                    // row-scale folds are twice the work: fold the first two
+                    // pieces between the loads so that the last load is issued
+                    // after two folds rather than three
+                    tmem_ld32(tbase + pcol(0), ra);
+                    tmem_ld32(tbase + pcol(1), rb);
+                    tmem_ld_wait_regs2(ra, rb);
+                    fold(0, ra);
+                    tmem_ld32(tbase + pcol(2), ra);
+                    fold(1, rb);
+                    tmem_ld32(tbase + pcol(3), rb);
+                    tmem_ld_wait_regs2(ra, rb);
+                    release();
+                    fold(2, ra);
+                    fold(3, rb);
                 } else {
                     // four loads, each overlapped with the fold of the previous one
                     tmem_ld32(tbase + pcol(0), ra);
