@@ -424,19 +424,23 @@ def run_ours(args, rank, world):
 
     stream = torch.cuda.current_stream()
 
-    # W warm-up steps, continued (one at a time) until the GPU has been busy
-    # for --min-warmup-s, so that its clocks have ramped up even when the
-    # timed region is short
-    t_warm = time.time()
-    n_warm = 0
-    while n_warm < args.warmup or (time.time() - t_warm < args.min_warmup_s and n_warm < 100000):
+    # W warm-up steps, then more (one at a time) until the GPU has been busy
+    # with them for --min-warmup-s, so that its clocks have ramped up even
+    # when the timed region is short
+    def one_step():
         flush_l2()
         for _, f in launches:
             f()
-        n_warm += 1
-        if n_warm >= args.warmup:
-            torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        one_step()
     torch.cuda.synchronize()
+    n_warm = args.warmup
+    t_warm = time.time()
+    while time.time() - t_warm < args.min_warmup_s and n_warm < 100000:
+        one_step()
+        torch.cuda.synchronize()
+        n_warm += 1
     if fb.get_device_error() != 0:
         raise RuntimeError("device error during warm-up")
 
