@@ -496,6 +496,7 @@ int fp8_gemm_blockscaled(const uint8_t *A, int64_t lda, const float *sa, int64_t
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
+    p.group_m = gemm::group_m_for(K);
     p.offs = nullptr;
     p.G = 0;
 
@@ -551,6 +552,7 @@ int fp8_grouped_gemm_moe(const uint8_t *A, int64_t lda, const float *sa, int64_t
     p.M = static_cast<int>(M_total);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
+    p.group_m = gemm::group_m_for(K);
     p.offs = group_offsets;
     p.G = G;
 
@@ -595,6 +597,7 @@ int fp8_gemm_ue8m0(const uint8_t *A, int64_t lda, const float *sa, int64_t ldsa,
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
     p.K = static_cast<int>(K);
+    p.group_m = gemm::group_m_for(K);
     const int forced = g_tile_n.load(std::memory_order_relaxed);
     const int BN = (forced == 192) ? 192 : 256;
     CUtensorMap tA, tB;
@@ -645,6 +648,7 @@ int fp8_grouped_gemm_moe_swiglu(const uint8_t *A, int64_t lda, const float *sa, 
     p.M = static_cast<int>(M_total);
     p.N = static_cast<int>(Nh);
     p.K = static_cast<int>(K);
+    p.group_m = gemm::group_m_for(K);
     p.tile_n = 128;
     p.b_rows = static_cast<int>(2 * Nh);
     p.offs = group_offsets;

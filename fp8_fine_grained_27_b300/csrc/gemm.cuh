@@ -56,7 +56,16 @@ namespace gemm {
 constexpr int BM = 128;
 constexpr int BK = 128;
 constexpr int kFirstPromoWarp = 4;
-constexpr int kGroupM = 16;      // raster: 16 M tiles share each sweep over N
+// Raster: group_m M tiles sweep N together, so that the tiles in flight share
+// their A panels, which stay in L2 for the whole sweep while each B panel is
+// read once per group.  The host picks 32 when the group's A panels
+// (32 x 128 rows x K bytes) fit in 32 MB, else 16: at K = 7168 that halves
+// the B re-reads; at K = 18432 a 32-tile group no longer stays in L2.
+constexpr int kGroupMSmall = 16, kGroupMLarge = 32;
+__host__ __device__ inline int group_m_for(int64_t K)
+{
+    return (int64_t(kGroupMLarge) * 128 * K <= (int64_t(32) << 20)) ? kGroupMLarge : kGroupMSmall;
+}
 constexpr int kMaxGroups = 1024; // grouped GEMM: experts per call
 constexpr int kMaxSmem = 232448; // dynamic shared memory per CTA on sm_103
 
@@ -122,6 +131,7 @@ struct Params {
     int M, N, K;         // M = rows of A (M_total when grouped); N = output columns
     int tile_n;          // output columns per tile (BN; SwiGLU: 128)
     int b_rows;          // rows of B per expert (N; SwiGLU: 2N)
+    int group_m;         // raster group (dense only; group_m_for(K))
     const int32_t *offs; // grouped: [G+1] row offsets (device)
     int G;
 };
@@ -139,10 +149,10 @@ __device__ __forceinline__ Tile tile_of(int t, const Params &p, const int *tile_
     const int num_n = (p.N + p.tile_n - 1) / p.tile_n;
     if constexpr (!GROUPED) {
         const int num_m = (p.M + BM - 1) / BM;
-        const int per_group = kGroupM * num_n;
+        const int per_group = p.group_m * num_n;
         const int g = t / per_group;
-        const int first_m = g * kGroupM;
-        const int gsize = min(num_m - first_m, kGroupM);
+        const int first_m = g * p.group_m;
+        const int gsize = min(num_m - first_m, p.group_m);
         const int local = t - g * per_group;
         const int mt = first_m + local % gsize;
         const int nt = local / gsize;

@@ -73,6 +73,7 @@ struct Params {
     void *C;
     int64_t ldc;
     int M, N, K;
+    int group_m;  // raster group, gemm::group_m_for(K)
 };
 
 // UE8M0 byte of a power-of-two FP32 scale (its exponent field; 2^-127 is the
@@ -115,10 +116,10 @@ __device__ __forceinline__ Tile tile_of(int t, const Params &p)
 {
     const int num_n = (p.N + BN - 1) / BN;
     const int num_m = (p.M + BM - 1) / BM;
-    const int per_group = gemm::kGroupM * num_n;
+    const int per_group = p.group_m * num_n;
     const int g = t / per_group;
-    const int first_m = g * gemm::kGroupM;
-    const int gsize = min(num_m - first_m, gemm::kGroupM);
+    const int first_m = g * p.group_m;
+    const int gsize = min(num_m - first_m, p.group_m);
     const int local = t - g * per_group;
     Tile r;
     r.m0 = (first_m + local % gsize) * BM;
