@@ -52,7 +52,11 @@ FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1
 PROFILES = os.path.join(ROOT, "profiles")
 # workload -> (ncu summary under profiles/, sources whose hash it records)
 GEMM_PROFILE = {"mla": ("gemm_kernel_mla_4096x2112x7168.md", ["gemm.cuh", "ptx.cuh"]),
-                "mla_ue8m0": ("mx_gemm_kernel_mla_ue8m0.md", ["mx.cuh", "ptx.cuh"])}
+                "ffn": ("gemm_kernel_ffn_16384x18432x7168.md", ["gemm.cuh", "ptx.cuh"]),
+                "dgrad": ("gemm_kernel_dgrad_16384x7168x18432.md", ["gemm.cuh", "ptx.cuh"]),
+                "wgrad": ("gemm_kernel_wgrad_2048x7168x16384.md", ["gemm.cuh", "ptx.cuh"]),
+                "mla_ue8m0": ("mx_gemm_kernel_mla_ue8m0.md", ["mx.cuh", "ptx.cuh"]),
+                "ffn_ue8m0": ("mx_gemm_kernel_ffn_ue8m0.md", ["mx.cuh", "ptx.cuh"])}
 
 
 def kernel_source_hash(files):
