@@ -60,6 +60,19 @@ def test_ragged_shapes(fb, orc, tile_n, M, N, K):
     _dense(fb, orc, a, w, out_dtype=torch.float32, what=f"{M}x{N}x{K} fp32")
 
 
+def test_raster_groups_with_a_partial_last_group(fb, orc, tile_n):
+    """40 M tiles at a K whose raster group is 32 tiles: one full group, a
+    partial group of 8, a ragged last tile, and a ragged last N tile.  Two rows
+    of every M tile (its first and last) are checked, plus a seeded sample."""
+    M, N, K = 40 * 128 - 37, 520, 256
+    a = synth.fill_bf16(synth.OUTLIER, synth.key(90, M), (M, K), 1.0, 0.01, 50.0, k2=synth.key(91, M))
+    w = synth.fill_bf16(synth.NORMAL, synth.key(92, N), (N, K), 0.02)
+    must = [r for t in range(40) for r in (t * 128, min(t * 128 + 127, M - 1))]
+    rows = sample_rows(M, 64, seed=10, must=must)
+    _dense(fb, orc, a, w, rows=rows, what="raster groups")
+    _dense(fb, orc, a, w, out_dtype=torch.float32, rows=rows, what="raster groups fp32")
+
+
 def test_mla_full(fb, orc, tile_n):
     """Both MLA down-projections, every output checked."""
     d = synth.mla()

@@ -104,6 +104,17 @@ def test_mx_ragged_shapes(fb, orc, mx_tile, M, N, K):
     _mx(fb, orc, a, w, out_dtype=torch.float32, what=f"{M}x{N}x{K} fp32")
 
 
+def test_mx_raster_groups_with_a_partial_last_group(fb, orc, mx_tile):
+    """40 M tiles at a K whose raster group is 32 tiles (one full group, a
+    partial one, ragged last M and N tiles); the first and last row of every M
+    tile plus a seeded sample are checked."""
+    M, N, K = 40 * 128 - 37, 520, 256
+    a = synth.fill_bf16(synth.OUTLIER, synth.key(93, M), (M, K), 1.0, 0.01, 50.0, k2=synth.key(94, M))
+    w = synth.fill_bf16(synth.NORMAL, synth.key(95, N), (N, K), 0.02)
+    must = [r for t in range(40) for r in (t * 128, min(t * 128 + 127, M - 1))]
+    _mx(fb, orc, a, w, rows=sample_rows(M, 64, seed=11, must=must), what="mx raster groups")
+
+
 def test_mx_mla_full(fb, orc, mx_tile):
     d = synth.mla()
     _mx(fb, orc, d["A"], np.concatenate([d["Wq"], d["Wkv"]]), what="mla")
