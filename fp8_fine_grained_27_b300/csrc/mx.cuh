@@ -73,7 +73,7 @@ struct Params {
     void *C;
     int64_t ldc;
     int M, N, K;
-    int group_m;  // raster group, gemm::group_m_for(K)
+    int group_m;  // raster group (M tiles sweeping N together)
 };
 
 // UE8M0 byte of a power-of-two FP32 scale (its exponent field; 2^-127 is the
@@ -246,7 +246,30 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t lanes = static_cast<uint32_t>(q * 32) << 16;
         uint32_t c = 0;
         bool ok = true;
+        // At the start of each tile the scale writers prefetch the next
+        // tile's scale rows into L2 (and the first tile's at kernel start):
+        // each chunk's scales are one dependent global load ahead of the
+        // MMAs, and a cold load from HBM made the writers gate the MMAs.
+        const int ptid = (warp - 4) * 32 + lane;  // 0..127
+        auto prefetch_scales = [&](int t) {
+            if (t >= total_tiles)
+                return;
+            const Tile tn = tile_of<BN>(t, p);
+            for (int i = ptid; i < num_kb * 4; i += 128) {
+                const int kb = i >> 2;
+                const int r = min(tn.m0 + (i & 3) * 32, p.M - 1);
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(p.sa + static_cast<int64_t>(kb) * p.ldsa + r));
+            }
+            const int nb0 = tn.n0 / 128, nb_last = min((tn.n0 + BN - 1) / 128, (p.N - 1) / 128);
+            for (int i = ptid; i < (nb_last - nb0 + 1) * ((num_kb + 31) / 32); i += 128) {
+                const int per = (num_kb + 31) / 32;
+                const int nb = nb0 + i / per, kb = (i % per) * 32;
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(p.sb + static_cast<int64_t>(nb) * p.ldsb + kb));
+            }
+        };
+        prefetch_scales(blockIdx.x);
         for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+            prefetch_scales(t + gridDim.x);
             const Tile tl = tile_of<BN>(t, p);
             int rows[4];
 #pragma unroll
