@@ -554,17 +554,8 @@ def run_e2e(args, step, torch, fb, launches, flops, world, dist):
     pinned = [(n, torch.from_numpy(np.ascontiguousarray(a)).pin_memory()) for n, a in step.host_inputs()]
     outs = step.d["C"]
     out_host = [torch.empty(c.shape, dtype=c.dtype).pin_memory() for c in outs]
-    targets = {}
-    if step.name in ("mla", "tiny", "ffn", "mla_ue8m0", "ffn_ue8m0"):
-        targets = {"A": step.d["A"], **{f"W{i}": w for i, w in enumerate(step.d["W"])}}
-    elif step.name == "wgrad":
-        targets = {"dY": step.d["dY"], "X": step.d["X"]}
-    elif step.name == "dgrad":
-        targets = {"dY": step.d["dY"], "W": step.d["W"]}
-    elif step.name == "moe_chain":
-        targets = {"X": step.d["X"]}
-    else:
-        targets = {"A": step.d["A"]}
+    # each uploaded activation lands in the device buffer of the same name
+    targets = {name: step.d[name] for name, _ in pinned}
     h2d = sum(p.numel() * p.element_size() for _, p in pinned)
     d2h = sum(o.numel() * o.element_size() for o in out_host)
     n = max(3, min(args.e2e_steps, args.steps))
