@@ -32,6 +32,13 @@
  *     are row-major.  Base pointers must be 16-byte aligned and every row
  *     pitch a multiple of 16 bytes (FP8BS_EALIGN otherwise).
  *   - The device must be sm_103 (FP8BS_EARCH otherwise).
+ *   - The GEMM calls are launched with programmatic stream serialisation:
+ *     their on-chip set-up may start while the kernel before them in the
+ *     stream is still running, but they wait on the device for that kernel
+ *     to complete (and its writes to be visible) before touching global
+ *     memory.  Stream order is therefore kept exactly as for an ordinary
+ *     launch; the quantisers of this library let the next kernel start its
+ *     set-up early.
  */
 #ifndef FP8BS_H
 #define FP8BS_H
