@@ -33,3 +33,25 @@ def test_workload_accounting():
     assert bench.gemm_flops("moe_chain") == 2.0 * 32768 * (4096 * 7168 + 7168 * 2048)
     assert abs(bench.quant_bytes("ffn") - (16384 * 7168 * (3 + 4 / 128) + 18432 * 7168 * (3 + 4 / 16384))) < 1
     assert bench.job_throughput(10.0, 2.0, 4) == 20.0
+
+
+def test_profile_links():
+    """Every ncu summary bench.py links for a roofline's traffic exists and gives
+    the source hash and a per-launch byte count in the form bench.py parses (a
+    hash that no longer matches the source makes bench.py print null)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    for workload, (name, sources) in bench.GEMM_PROFILE.items():
+        text = open(os.path.join(ROOT, "profiles", name)).read()
+        fields = dict(l.split(":", 1) for l in text.splitlines()
+                      if l.startswith(("kernel_source_sha256_16:", "traffic_bytes_per_launch:")))
+        assert set(fields) == {"kernel_source_sha256_16", "traffic_bytes_per_launch"}, name
+        assert int(fields["traffic_bytes_per_launch"].split()[0]) > 0
+        assert "ncu " in text and "--clock-control none" in text, name
+        assert len(fields["kernel_source_sha256_16"].split()[0]) == 16, name
+
+
+def test_every_profile_gives_its_command():
+    for name in os.listdir(os.path.join(ROOT, "profiles")):
+        text = open(os.path.join(ROOT, "profiles", name)).read()
+        assert "python bench.py" in text and "ncu " in text and "--clock-control none" in text, name
