@@ -71,6 +71,14 @@ def test_status_strings_and_argument_errors(libpath):
     assert L.fp8_grouped_gemm_moe(vp(16), 128, vp(16), 4, vp(16), vp(16), vp(16), 0, 4, vp(16), 8, 0,
                                   8, 128, None) == b.EINVAL  # G = 0
     assert L.fp8bs_selftest_timeout(0, None) == b.EINVAL
+    # sizes past the 32-bit tile indexing are refused before any launch
+    big = 1 << 31
+    assert L.fp8_gemm_blockscaled(vp(16), 128, vp(16), big, vp(16), 128, vp(16), 1, 0, vp(16), 8, 0,
+                                  big, 8, 128, None) == b.EINVAL
+    assert L.fp8_gemm_ue8m0(vp(16), 128, vp(16), 4, vp(16), big, vp(16), 1, vp(16), big, 0,
+                            4, big, 128, None) == b.EINVAL
+    assert L.fp8_quant_1x128(vp(16), big + 1, 128, 128, 0, vp(16), 128, vp(16), big + 1, None) == b.EINVAL
+    assert L.fp8_quant_128x128(vp(16), big + 1, 128, 128, vp(16), 128, vp(16), 1, None) == b.EINVAL
     # empty problems are a successful no-op
     assert L.fp8_gemm_blockscaled(None, 128, None, 4, None, 128, None, 1, 0, None, 8, 0,
                                   0, 8, 128, None) == b.OK
