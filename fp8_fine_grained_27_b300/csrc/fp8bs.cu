@@ -30,12 +30,15 @@ namespace fp8bs {
 __global__ void selftest_timeout_kernel(uint64_t limit_ns)
 {
     __shared__ __align__(8) uint64_t bar;
+    __shared__ int s_abort;
     const uint32_t a = smem_addr(&bar);
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0) {
+        s_abort = 0;
         mbar_init(a, 1);
+    }
     __syncthreads();
     if (threadIdx.x == 0)
-        mbar_wait(a, 0, ERR_TIMEOUT_SELFTEST, limit_ns);
+        mbar_wait(a, 0, ERR_TIMEOUT_SELFTEST, &s_abort, limit_ns);
     __syncthreads();
 }
 

@@ -321,8 +321,11 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
     const uint32_t bar_xch = bar_tempty + 8 * NTMEM;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_TMEMSLOT);
     int *tile_start = reinterpret_cast<int *>(smem + L::OFF_TILESTART);
+    // raised by the first wait of this CTA that gives up (see mbar_wait)
+    __shared__ int s_abort;
 
     if (threadIdx.x == 0) {
+        s_abort = 0;
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
@@ -376,7 +379,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                 for (int kb = 0; kb < num_kb; ++kb, ++c) {
                     const int s = c % STAGES;
                     const uint32_t ph = (c / STAGES) & 1;
-                    if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, ERR_TIMEOUT_PRODUCER)) {
+                    if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, ERR_TIMEOUT_PRODUCER, &s_abort)) {
                         ok = false;
                         break;
                     }
@@ -390,7 +393,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                         tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, kb * BK, tl.brow0, bar_full + 8 * s);
                     }
                     if constexpr (BMODE == 1) {
-                        if (!mbar_wait(bar_sbempty + 8 * s, ph ^ 1, ERR_TIMEOUT_PRODUCER)) {
+                        if (!mbar_wait(bar_sbempty + 8 * s, ph ^ 1, ERR_TIMEOUT_PRODUCER, &s_abort)) {
                             ok = false;
                             break;
                         }
@@ -404,7 +407,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                 // let copies already issued land before the CTA exits
                 const uint32_t issued = c;
                 for (uint32_t d = (issued > STAGES ? issued - STAGES : 0); d < issued; ++d)
-                    mbar_wait(bar_full + 8 * (d % STAGES), (d / STAGES) & 1, ERR_TIMEOUT_PRODUCER, 100000000ull);
+                    mbar_wait(bar_full + 8 * (d % STAGES), (d / STAGES) & 1, ERR_TIMEOUT_PRODUCER, &s_abort, 100000000ull);
             }
         } else if ((warp == 1 || warp == 3) && lane == 0) {
             // -------------------------------------------------------- MMA issuers
@@ -420,8 +423,8 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                     const uint32_t ph = (c / STAGES) & 1;
                     const int b = c % NTMEM;
                     const uint32_t tph = (c / NTMEM) & 1;
-                    if (!mbar_wait(bar_tempty + 8 * b, tph ^ 1, ERR_TIMEOUT_MMA) ||
-                        !mbar_wait(bar_full + 8 * s, ph, ERR_TIMEOUT_MMA)) {
+                    if (!mbar_wait(bar_tempty + 8 * b, tph ^ 1, ERR_TIMEOUT_MMA, &s_abort) ||
+                        !mbar_wait(bar_full + 8 * s, ph, ERR_TIMEOUT_MMA, &s_abort)) {
                         ok = false;
                         break;
                     }
@@ -443,7 +446,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                     --d;
                 if (d > 0) {
                     --d;
-                    mbar_wait(bar_tfull + 8 * (d % NTMEM), (d / NTMEM) & 1, ERR_TIMEOUT_MMA, 100000000ull);
+                    mbar_wait(bar_tfull + 8 * (d % NTMEM), (d / NTMEM) & 1, ERR_TIMEOUT_MMA, &s_abort, 100000000ull);
                 }
             }
         }
@@ -491,9 +494,9 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                 const int s = c % STAGES;
                 // every lane waits, then the warp reconverges before the
                 // .sync.aligned TMEM loads
-                bool got = mbar_wait(bar_tfull + 8 * b, tph, ERR_TIMEOUT_CONSUMER);
+                bool got = mbar_wait(bar_tfull + 8 * b, tph, ERR_TIMEOUT_CONSUMER, &s_abort);
                 if constexpr (BMODE == 1)
-                    got = got && mbar_wait(bar_sbfull + 8 * s, (c / STAGES) & 1, ERR_TIMEOUT_CONSUMER);
+                    got = got && mbar_wait(bar_sbfull + 8 * s, (c / STAGES) & 1, ERR_TIMEOUT_CONSUMER, &s_abort);
                 if (!__all_sync(0xFFFFFFFFu, got))
                     return false;
                 tc_fence_after();
@@ -643,7 +646,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                 float *xch = reinterpret_cast<float *>(smem + L::OFF_XCH) + (tcount & 1) * 256;
                 xch[grp * 128 + row] = am;
                 mbar_arrive(bar_xch);
-                const bool got = mbar_wait(bar_xch, tcount & 1, ERR_TIMEOUT_CONSUMER);
+                const bool got = mbar_wait(bar_xch, tcount & 1, ERR_TIMEOUT_CONSUMER, &s_abort);
                 if (!__all_sync(0xFFFFFFFFu, got)) {
                     ok = false;
                     break;

@@ -146,8 +146,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t bar_tfull = bar_sffull + 8 * STAGES;
     const uint32_t bar_tempty = bar_tfull + 8 * NACC;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_TMEMSLOT);
+    // raised by the first wait of this CTA that gives up (see mbar_wait)
+    __shared__ int s_abort;
 
     if (threadIdx.x == 0) {
+        s_abort = 0;
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
@@ -187,7 +190,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int kb = 0; kb < num_kb; ++kb, ++c) {
                     const int s = c % STAGES;
                     const uint32_t ph = (c / STAGES) & 1;
-                    if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, ERR_TIMEOUT_PRODUCER)) {
+                    if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, ERR_TIMEOUT_PRODUCER, &s_abort)) {
                         ok = false;
                         break;
                     }
@@ -198,7 +201,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (!ok) {  // let copies already issued land before the CTA exits
                 for (uint32_t d = (c > STAGES ? c - STAGES : 0); d < c; ++d)
-                    mbar_wait(bar_full + 8 * (d % STAGES), (d / STAGES) & 1, ERR_TIMEOUT_PRODUCER, 100000000ull);
+                    mbar_wait(bar_full + 8 * (d % STAGES), (d / STAGES) & 1, ERR_TIMEOUT_PRODUCER, &s_abort, 100000000ull);
             }
         }
     } else if (warp == 1) {
@@ -209,7 +212,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++tcount) {
                 // accumulator b must have been drained by the epilogue of the tile NACC before
                 const int b = tcount % NACC;
-                if (!mbar_wait(bar_tempty + 8 * b, ((tcount / NACC) & 1) ^ 1, ERR_TIMEOUT_MMA)) {
+                if (!mbar_wait(bar_tempty + 8 * b, ((tcount / NACC) & 1) ^ 1, ERR_TIMEOUT_MMA, &s_abort)) {
                     ok = false;
                     break;
                 }
@@ -218,8 +221,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int kb = 0; kb < num_kb; ++kb, ++c) {
                     const int s = c % STAGES;
                     const uint32_t ph = (c / STAGES) & 1;
-                    if (!mbar_wait(bar_full + 8 * s, ph, ERR_TIMEOUT_MMA) ||
-                        !mbar_wait(bar_sffull + 8 * s, ph, ERR_TIMEOUT_MMA)) {
+                    if (!mbar_wait(bar_full + 8 * s, ph, ERR_TIMEOUT_MMA, &s_abort) ||
+                        !mbar_wait(bar_sffull + 8 * s, ph, ERR_TIMEOUT_MMA, &s_abort)) {
                         ok = false;
                         break;
                     }
@@ -237,7 +240,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             if (!ok && c > 0)  // the last committed chain completes before TMEM is freed
-                mbar_wait(bar_empty + 8 * ((c - 1) % STAGES), ((c - 1) / STAGES) & 1, ERR_TIMEOUT_MMA,
+                mbar_wait(bar_empty + 8 * ((c - 1) % STAGES), ((c - 1) / STAGES) & 1, ERR_TIMEOUT_MMA, &s_abort,
                           100000000ull);
         }
     } else if (warp >= 4 && warp < 8) {
@@ -292,7 +295,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     bw[g] = (g < BN / 32) ? ue8m0_word(__ldg(p.sb + static_cast<int64_t>(nbg[g < BN / 32 ? g : 0]) * p.ldsb + kb))
                                           : 0x7F7F7F7Fu;
                 // the slot is free once the MMAs that read it (chunk c - STAGES) completed
-                const bool got = mbar_wait(bar_empty + 8 * s, ph ^ 1, ERR_TIMEOUT_CONSUMER);
+                const bool got = mbar_wait(bar_empty + 8 * s, ph ^ 1, ERR_TIMEOUT_CONSUMER, &s_abort);
                 if (!__all_sync(0xFFFFFFFFu, got)) {
                     ok = false;
                     break;
@@ -317,7 +320,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++tcount) {
             const Tile tl = tile_of<BN>(t, p);
             const int b = tcount % NACC;
-            const bool got = mbar_wait(bar_tfull + 8 * b, (tcount / NACC) & 1, ERR_TIMEOUT_CONSUMER);
+            const bool got = mbar_wait(bar_tfull + 8 * b, (tcount / NACC) & 1, ERR_TIMEOUT_CONSUMER, &s_abort);
             if (!__all_sync(0xFFFFFFFFu, got))
                 break;
             tc_fence_after();

@@ -62,16 +62,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 }
 
 // Device error word shared by every kernel of the library (the library is a
-// single translation unit, so this is its one definition).
+// single translation unit, so this is its one definition).  Kernels only
+// write it (first error wins); fp8bs_get_device_error reads and clears it.
 __device__ int g_fp8bs_error = 0;
 
 enum : int { ERR_NONE = 0, ERR_TIMEOUT_PRODUCER = 1, ERR_TIMEOUT_MMA = 2,
              ERR_TIMEOUT_CONSUMER = 3, ERR_TIMEOUT_SELFTEST = 4 };
 
 // Bounded wait on an mbarrier phase.  Spins briefly, then checks the global
-// timer; after `limit_ns` (or as soon as another role of the kernel has
-// recorded an error) it records `code` (first error wins) and returns false.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int code,
+// timer.  `abort` is a flag in the CTA's shared memory (zeroed at the CTA's
+// start): after `limit_ns` the wait records `code` in the device error word
+// (first error wins), raises the flag and returns false; any wait of the same
+// CTA that sees the flag raised returns false at once, so the other roles of
+// a CTA give up together.  The flag belongs to one CTA of one launch, so an
+// error that an earlier launch left in the device error word does not make
+// later launches give up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int code, volatile int *abort,
                                           uint64_t limit_ns = 2000000000ull)
 {
 #pragma unroll 1
@@ -83,10 +89,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int cod
     while (true) {
         if (mbar_try_wait(bar, parity))
             return true;
-        if (*reinterpret_cast<volatile int *>(&g_fp8bs_error) != 0)
+        if (*abort != 0)
             return false;
         if (globaltimer_ns() - t0 > limit_ns) {
             atomicCAS(&g_fp8bs_error, 0, code);
+            *abort = 1;
             return false;
         }
     }

@@ -27,7 +27,9 @@
  *   - Argument errors are returned synchronously before any launch.  A failed
  *     launch returns FP8BS_ECUDA.  A kernel that gives up on a bounded
  *     internal wait records FP8BS_ETIMEOUT in a device error word read by
- *     fp8bs_get_device_error.
+ *     fp8bs_get_device_error; the outputs of that launch are then incomplete.
+ *     The word only reports: a launch gives up on its own waits alone, so an
+ *     error left unread by an earlier launch does not affect later ones.
  *   - Leading dimensions (ld*) are in elements.  Code and BF16/FP32 matrices
  *     are row-major.  Base pointers must be 16-byte aligned and every row
  *     pitch a multiple of 16 bytes (FP8BS_EALIGN otherwise).
@@ -335,8 +337,9 @@ const char *fp8bs_status_string(int status);
 
 /*
  * fp8bs_get_device_error -- synchronise `stream`, read and clear the device
- * error word of the current device.  Returns FP8BS_OK, FP8BS_ETIMEOUT (a
- * kernel abandoned a bounded wait), or FP8BS_ECUDA.
+ * error word of the current device.  Returns FP8BS_OK, FP8BS_ETIMEOUT (some
+ * kernel since the last read abandoned a bounded wait, and its outputs are
+ * incomplete), or FP8BS_ECUDA.
  */
 int fp8bs_get_device_error(void *stream);
 

@@ -251,6 +251,28 @@ def test_timeout_path_reports_and_recovers(fb):
     assert int(q[0, 0]) == 0x7E and float(s[0, 0]) == float(np.float32(1) / np.float32(448))
 
 
+def test_gemm_after_an_uncleared_timeout_is_complete(fb, orc):
+    """A timeout recorded by an earlier launch and not yet read does not make
+    later launches give up: a GEMM run after it is complete and correct, the
+    earlier error is still reported once, and the word is then clear."""
+    fb.selftest_timeout(1_000_000)
+    d = synth.tiny()
+    _dense_no_error_check(fb, orc, d["A"], d["B"])
+    assert fb.get_device_error() == fb.binding.ETIMEOUT
+    assert fb.get_device_error() == 0
+
+
+def _dense_no_error_check(fb, orc, a_bits, w_bits):
+    qa, sa = fb.quant_1x128(dev(a_bits))
+    qb, sb = fb.quant_128x128(dev(w_bits))
+    C = fb.gemm_blockscaled(qa, sa, qb, sb, 0)
+    torch.cuda.synchronize()
+    oqa, osa = orc.quant_1x128_rows(a_bits)
+    oqb, osb = orc.quant_128x128(w_bits)
+    ref = orc.bf16_round(orc.gemm_blockscaled(oqa, osa, oqb, osb, 0))
+    assert_gemm_close(host_bits(C), ref, "after an uncleared timeout")
+
+
 def test_mla_stacked_weight_equals_separate(fb, orc):
     """W_q (1536 rows) and W_kv (576 rows) stacked into one 2112-row weight:
     the 128x128 blocks never straddle the two, so the stacked quantisation and
