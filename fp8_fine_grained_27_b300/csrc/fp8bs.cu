@@ -22,6 +22,8 @@
 // calls that use it on one device must be ordered (one stream, or events).
 static constexpr long long kRouteScratchBytes = 4096;
 static __device__ __align__(256) unsigned char g_route_scratch[kRouteScratchBytes];
+static_assert(kRouteScratchBytes >= ((fp8bs::moe::kMaxExperts * 4 + 255) / 256) * 256,
+              "the static routing scratch must hold the workspace of the largest expert count");
 
 namespace fp8bs {
 
