@@ -2,12 +2,14 @@
 """Benchmark: fine-grained FP8 (E4M3) quantise + block-scaled GEMM steps on B300.
 
 One step = one pass of the whole hot path over one batch of the workload:
-  mla   (default) A 4096x7168 BF16 -> 1x128 quantise; W_q 1536x7168 and
+  ffn   (default) A 16384x7168 (Student-t), B 18432x7168: quantise both
+        (one launch), one GEMM 16384x18432x7168 with BF16 output.  The
+        largest dense GEMM of the pages' model, and the primary GEMM number.
+  mla   A 4096x7168 BF16 -> 1x128 quantise; W_q 1536x7168 and
         W_kv 576x7168 stored stacked as one 2112x7168 weight (1536 is a
         multiple of 128, so no 128x128 block straddles the two) -> one
         128x128 quantise and one GEMM whose column slices [0,1536) and
         [1536,2112) are the q and kv latents (BF16 out).
-  ffn   A 16384x7168 (Student-t), B 18432x7168: quantise both, one GEMM.
   wgrad dY 16384x2048, X 16384x7168: token-wise 1x128 quantise (transposed
         codes), dW = dY^T X with FP32 output.
   dgrad dY 16384x18432, W 18432x7168: dY 1x128 and W's transposed 128x128
@@ -24,7 +26,11 @@ In the mla/ffn steps one launch quantises both the activation and the weight.
 Inputs are seeded synthetic tensors (synth/), resident in HBM before timing.
 L2 is flushed before every timed step, outside the step's CUDA events: a 256 MB
 write, then a 256 MB read that evicts the dirty lines the write left
-(--flush-mode write keeps only the write).  Prints one JSON line (rank 0).
+(--flush-mode write keeps only the write).  The warm-up runs back to back
+(a few steps queued ahead of the GPU, no synchronisation per step) for at
+least --min-warmup-s and goes straight into the timed steps, so the GPU is
+under steady load when timing starts; the clock sampler runs from before the
+warm-up.  Prints one JSON line (rank 0).
 
 --impl reference times the CPU oracle (oracle/) on a bounded sample of the
 same workload instead: the method's plain restatement on the host cores.
@@ -112,7 +118,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
             return
@@ -123,16 +129,22 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append((time.time(), line.strip()))
 
-    def stop(self, t0, t1):
+    def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.25)
+            return
+        time.sleep(0.1)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        rows = [l for (ts, l) in self.lines if t0 - 0.15 <= ts <= t1 + 0.15] or [l for _, l in self.lines]
+
+    def summary(self, t0, t1):
+        """Median SM clock, maximum and active throttle reasons of the samples
+        taken between wall times t0 and t1 (all samples if none fall inside)."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = [l for (ts, l) in self.lines if t0 - 0.05 <= ts <= t1 + 0.05] or [l for _, l in self.lines]
         mhz, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for l in rows:
@@ -185,6 +197,16 @@ def workload_desc(name):
         "tiny": {"workload": "tiny", "M": 128, "K": 512, "N": [256], "gemms": 1,
                  "quant": "A 1x128, B 128x128", "out": "bf16"},
     }[name]
+
+
+METRIC = "block-scaled FP8 GEMM TFLOPS (% of B300 FP8 peak); quantize GB/s (% HBM)"
+
+
+def bench_config(args, world):
+    """The `config` object of both arms' lines (same keys, same values)."""
+    return {**workload_desc(args.workload),
+            "l2": f"flushed ({args.flush_mb} MB {args.flush_mode}) before every step",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
 # kernels one labelled C-ABI call launches (fp8_moe_route: logits, selection, grouping)
@@ -428,42 +450,40 @@ def run_ours(args, rank, world):
 
     stream = torch.cuda.current_stream()
 
-    # W warm-up steps, then more (one at a time) until the GPU has been busy
-    # with them for --min-warmup-s, so that its clocks have ramped up even
-    # when the timed region is short
     def one_step():
         flush_l2()
         for _, f in launches:
             f()
 
-    for _ in range(args.warmup):
-        one_step()
-    torch.cuda.synchronize()
-    n_warm = args.warmup
-    t_warm = time.time()
-    while time.time() - t_warm < args.min_warmup_s and n_warm < 100000:
-        one_step()
-        torch.cuda.synchronize()
-        n_warm += 1
-    if fb.get_device_error() != 0:
-        raise RuntimeError("device error during warm-up")
-
     nk = len(launches)
-    # The timed region: each step's launches go out back to back, as a caller
-    # issues them, with events only around the step.  A second pass over the
-    # same number of steps puts events between the launches, for the
-    # per-kernel split (an event between two launches keeps the GEMM's set-up
-    # from overlapping the quantiser before it, so that pass is not the step
-    # time).
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     evk = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
-    time.sleep(0.3)
+    # Warm-up: W steps, then more until --min-warmup-s of wall time has passed,
+    # issued back to back.  At most QUEUE steps are in flight ahead of the
+    # host (it waits on the event of an earlier step, not on the device), so
+    # the wall time tracks the GPU's and the GPU never idles between steps.
+    # The timed steps follow straight after (the barrier and synchronisation
+    # around them are the only gap), so they run under the same steady load.
+    QUEUE = 4
+    inflight = []
+    n_warm = 0
+    t_warm = time.time()
+    while n_warm < args.warmup or (time.time() - t_warm < args.min_warmup_s and n_warm < 100000):
+        one_step()
+        e = torch.cuda.Event()
+        e.record(stream)
+        inflight.append(e)
+        if len(inflight) > QUEUE:
+            inflight.pop(0).synchronize()
+        n_warm += 1
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
+    # The timed region: each step's launches go out back to back, as a caller
+    # issues them, with events only around the step.
     for k in range(args.steps):
         flush_l2()
         ev[k][0].record(stream)
@@ -474,6 +494,12 @@ def run_ours(args, rank, world):
     if dist:
         dist.barrier()
     t1 = time.time()
+    if fb.get_device_error() != 0:
+        raise RuntimeError("device error during the warm-up or the timed region")
+    # A second pass over the same number of steps puts events between the
+    # launches, for the per-kernel split (an event between two launches keeps
+    # the GEMM's set-up from overlapping the quantiser before it, so that pass
+    # is not the step time).
     for k in range(args.steps):
         flush_l2()
         evk[k][0].record(stream)
@@ -482,9 +508,12 @@ def run_ours(args, rank, world):
             evk[k][j + 1].record(stream)
     torch.cuda.synchronize()
     t2 = time.time()
-    clocks = sampler.stop(t0, t2)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+    clocks_split = sampler.summary(t1, t2)
+    clocks_warm = sampler.summary(t_warm, t0)
     if fb.get_device_error() != 0:
-        raise RuntimeError("device error during the timed region")
+        raise RuntimeError("device error during the per-kernel pass")
 
     per_step = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)]
     per_kernel = {}
@@ -513,15 +542,22 @@ def run_ours(args, rank, world):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = run_cpu_baseline(args.workload, budget_s=args.cpu_budget)
 
+    first, last = per_step[:5], per_step[-5:]
     line = {
-        "metric": "block-scaled FP8 GEMM TFLOPS (% of B300 FP8 peak); quantize GB/s (% HBM)",
+        "metric": METRIC,
         "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "warmup_steps_run": n_warm, "ms_per_step": round(ms_step, 5),
-        "ms_per_step_median": round(float(np.median(per_step)), 5), "higher_is_better": True,
+        "warmup": args.warmup, "warmup_steps_run": n_warm, "warmup_s": round(t0 - t_warm, 3),
+        "ms_per_step": round(ms_step, 5),
+        "ms_per_step_median": round(float(np.median(per_step)), 5),
+        # the spread of the timed steps: a ramp (first steps slower than the
+        # last) would show here
+        "per_step_ms": {"first5_median": round(float(np.median(first)), 5),
+                        "last5_median": round(float(np.median(last)), 5),
+                        "min": round(float(min(per_step)), 5), "max": round(float(max(per_step)), 5)},
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> fp32 accumulate",
         "data": "synthetic (seeded; shapes of the DeepSeek-V3 pages)",
-        "config": {**workload_desc(args.workload), "l2": f"flushed ({args.flush_mb} MB {args.flush_mode}) before every step",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": bench_config(args, world),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(fp8_peak, 1),
                      "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
                      "traffic": profiled_traffic(args.workload),
@@ -539,6 +575,11 @@ def run_ours(args, rank, world):
         "e2e": e2e,
         "gpu_launches": sum(KERNELS_PER_CALL.get(l, 1) for l, _ in launches) * args.steps,
         "clocks": clocks,
+        # the same sampler over the warm-up and over the per-kernel pass, and
+        # the step time in SM clock cycles at the timed region's median clock
+        "clocks_bins": {"warmup": clocks_warm, "per_kernel_pass": clocks_split,
+                        "step_kcycles_at_median_mhz": (round(ms_step * clocks["sm_mhz"], 1)
+                                                       if clocks.get("sm_mhz") else None)},
         "wall_s_timed_region": round(t1 - t0, 3),
         "cpu_baseline": cpu,
     }
@@ -720,11 +761,11 @@ def run_reference(args, rank, world):
     value = flops / (ms * 1e-3) / 1e12
     line = {
         "impl": "reference",
-        "metric": "block-scaled FP8 GEMM TFLOPS (% of B300 FP8 peak); quantize GB/s (% HBM)",
+        "metric": METRIC,
         "value": round(value, 8), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 codes, f64 chunk sums, f32 promotion", "data": "synthetic (seeded)",
-        "config": workload_desc(args.workload),
+        "config": bench_config(args, world),
         "cpu_baseline": {"value": round(value, 8), "unit": "TFLOP/s", "cores": oracle.nthreads(),
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 8), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -737,11 +778,12 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
-    ap.add_argument("--workload", default="mla", choices=["mla", "ffn", "wgrad", "dgrad", "moe", "moe_chain", "tiny",
+    ap.add_argument("--workload", default="ffn", choices=["mla", "ffn", "wgrad", "dgrad", "moe", "moe_chain", "tiny",
                                                         "mla_ue8m0", "ffn_ue8m0"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
-    ap.add_argument("--min-warmup-s", type=float, default=0.5, help="keep warming up until this long has passed")
+    ap.add_argument("--min-warmup-s", type=float, default=1.0,
+                    help="keep warming up (back to back) until this long has passed")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--flush-mb", type=int, default=256, help="L2 flush buffer (> 126 MB L2)")
