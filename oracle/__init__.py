@@ -81,6 +81,8 @@ def lib():
         L.orc_route_logits.restype = None
         L.orc_route_select.argtypes = [vp, i64, i64, vp, i32, vp, vp]
         L.orc_route_select.restype = None
+        L.orc_route_gates.argtypes = [vp, i64, i64, vp, i32, vp]
+        L.orc_route_gates.restype = None
         L.orc_route_permute.argtypes = [vp, i64, i32, i64, vp, vp, vp]
         L.orc_route_permute.restype = None
         L.orc_swiglu_quant.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, i32]
@@ -247,22 +249,23 @@ def grouped_gemm(A: np.ndarray, sa: np.ndarray, B: np.ndarray, sb: np.ndarray,
 # --- the MoE chain (V3 report §2 DeepSeekMoE, §4 aux-loss-free routing) ----
 
 def route_logits(x_bf16: np.ndarray, centroids: np.ndarray, threads: int | None = None) -> np.ndarray:
-    """Affinity logits l[t, e] = u_t . c_e in FP32, one fused multiply-add per term in k
-    order.  x_bf16: uint16 [T, D]; centroids: f32 [E, D].  Returns f32 [T, E]."""
+    """Affinity logits l[t, e] = u_t . c_e in double (exact products, a double sum:
+    within D * 2^-53 * sum|u c| of the exact value).  x_bf16: uint16 [T, D];
+    centroids: f32 [E, D].  Returns f64 [T, E]."""
     x = _c(x_bf16, np.uint16)
     c = _c(centroids, np.float32)
     T, D = x.shape
     E = c.shape[0]
-    out = np.empty((T, E), np.float32)
+    out = np.empty((T, E), np.float64)
     lib().orc_route_logits(_p(x), T, D, D, _p(c), D, E, _p(out), threads or nthreads())
     return out
 
 
 def route_select(logits: np.ndarray, bias: np.ndarray, topk: int):
     """Top-k experts per token by sigmoid(l) + b (double; ties to the lower index), listed in
-    increasing expert order, with gates s_e / sum of the chosen s.  Returns (sel int32 [T, k],
-    gate f32 [T, k])."""
-    l = _c(logits, np.float32)
+    increasing expert order, with gates s_e / sum of the chosen s.  logits: [T, E] (taken as
+    double).  Returns (sel int32 [T, k], gate f32 [T, k])."""
+    l = _c(logits, np.float64)
     b = _c(bias, np.float32)
     T, E = l.shape
     assert 0 < topk <= E
@@ -270,6 +273,18 @@ def route_select(logits: np.ndarray, bias: np.ndarray, topk: int):
     gate = np.empty((T, topk), np.float32)
     lib().orc_route_select(_p(l), T, E, _p(b), topk, _p(sel), _p(gate))
     return sel, gate
+
+
+def route_gates(logits: np.ndarray, sel: np.ndarray):
+    """Gates of a given selection sel int32 [T, k]: s_e / sum of the chosen s (double, in
+    the listed order), rounded to f32.  logits: [T, E] (taken as double)."""
+    l = _c(logits, np.float64)
+    sl = _c(sel, np.int32)
+    T, E = l.shape
+    k = sl.shape[1]
+    gate = np.empty((T, k), np.float32)
+    lib().orc_route_gates(_p(l), T, E, _p(sl), k, _p(gate))
+    return gate
 
 
 def route_permute(sel: np.ndarray, E: int):

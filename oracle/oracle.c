@@ -425,16 +425,18 @@ void orc_e4m3_encode_patterns(uint64_t lo, int64_t n, uint8_t *q, int nthreads)
 /* normalised over the selected experts).                                   */
 /* ======================================================================== */
 
-/* Affinity logits l[t][e] = u_t . c_e in FP32: one fused multiply-add per  */
-/* term, in k order.  The routing decision is taken in this precision and   */
-/* order on both sides (the kernel's), so the logits are reproducible bit   */
-/* for bit.  x: BF16 [T][ldx] (D used); c: FP32 [E][ldc]; l: FP32 [T][E].   */
+/* Affinity logits l[t][e] = u_t . c_e, the token-centroid product inside  */
+/* the sigmoid of [V3-report] §4, in double: every product of a BF16 and an */
+/* FP32 value is exact in double (8 + 24 significant bits), and the sum of  */
+/* D of them in double is within D * 2^-53 * sum |u c| of the exact value,  */
+/* far below any FP32 evaluation.  No summation order of a GPU kernel is    */
+/* adopted.  x: BF16 [T][ldx] (D used); c: FP32 [E][ldc]; l: double [T][E].*/
 typedef struct {
     const uint16_t *x;
     int64_t D, ldx;
     const float *c;
     int64_t ldc, E;
-    float *l;
+    double *l;
 } rl_ctx;
 
 static void rl_token(void *p, int64_t t)
@@ -443,34 +445,47 @@ static void rl_token(void *p, int64_t t)
     const uint16_t *u = c->x + t * c->ldx;
     for (int64_t e = 0; e < c->E; ++e) {
         const float *ce = c->c + e * c->ldc;
-        float acc = 0.0f;
+        double acc = 0.0;
         for (int64_t k = 0; k < c->D; ++k)
-            acc = fmaf(bf16_to_f32(u[k]), ce[k], acc);
+            acc += (double)bf16_to_f32(u[k]) * (double)ce[k];
         c->l[t * c->E + e] = acc;
     }
 }
 
 void orc_route_logits(const uint16_t *x, int64_t T, int64_t D, int64_t ldx,
-                      const float *c, int64_t ldc, int64_t E, float *l, int nthreads)
+                      const float *c, int64_t ldc, int64_t E, double *l, int nthreads)
 {
     rl_ctx ctx = {x, D, ldx, c, ldc, E, l};
     parallel_for(T, nthreads, rl_token, &ctx);
 }
 
+/* Gates of a given selection: fl32(s_e / sum of the chosen s) with        */
+/* s_e = 1 / (1 + exp(-l_e)), the sum taken over the chosen experts in the  */
+/* order listed, in double ([V3-report] §4: the gate is the affinity        */
+/* normalised over the selected experts).                                   */
+void orc_route_gates(const double *l, int64_t T, int64_t E, const int32_t *sel, int topk, float *gate)
+{
+    for (int64_t t = 0; t < T; ++t) {
+        double sum = 0.0;
+        for (int j = 0; j < topk; ++j)
+            sum += 1.0 / (1.0 + exp(-l[t * E + sel[t * topk + j]]));
+        for (int j = 0; j < topk; ++j)
+            gate[t * topk + j] = (float)((1.0 / (1.0 + exp(-l[t * E + sel[t * topk + j]]))) / sum);
+    }
+}
+
 /* Selection: affinity s_e = 1 / (1 + exp(-l_e)) and key_e = s_e + b_e in   */
 /* double; the top-k keys win, a tie going to the lower expert index.  The  */
 /* chosen experts are listed in increasing index order; their gates are     */
-/* fl32(s_e / sum of the chosen s), the sum taken in that order in double.  */
-void orc_route_select(const float *l, int64_t T, int64_t E, const float *bias, int topk,
+/* those of orc_route_gates.                                                */
+void orc_route_select(const double *l, int64_t T, int64_t E, const float *bias, int topk,
                       int32_t *sel, float *gate)
 {
     double *key = (double *)malloc((size_t)E * sizeof(double));
-    double *s = (double *)malloc((size_t)E * sizeof(double));
     char *taken = (char *)malloc((size_t)E);
     for (int64_t t = 0; t < T; ++t) {
         for (int64_t e = 0; e < E; ++e) {
-            s[e] = 1.0 / (1.0 + exp(-(double)l[t * E + e]));
-            key[e] = s[e] + (double)bias[e];
+            key[e] = 1.0 / (1.0 + exp(-l[t * E + e])) + (double)bias[e];
             taken[e] = 0;
         }
         for (int j = 0; j < topk; ++j) {
@@ -483,17 +498,12 @@ void orc_route_select(const float *l, int64_t T, int64_t E, const float *bias, i
             taken[best] = 1;
         }
         int j = 0;
-        double sum = 0.0;
         for (int64_t e = 0; e < E; ++e)
-            if (taken[e]) {
+            if (taken[e])
                 sel[t * topk + j++] = (int32_t)e;
-                sum += s[e];
-            }
-        for (j = 0; j < topk; ++j)
-            gate[t * topk + j] = (float)(s[sel[t * topk + j]] / sum);
     }
+    orc_route_gates(l, T, E, sel, topk, gate);
     free(key);
-    free(s);
     free(taken);
 }
 

@@ -1,16 +1,25 @@
 """GPU parity of the routed-expert chain (V3 report §2 DeepSeekMoE, §4 aux-loss-free
 routing) against the oracle, through the C ABI.
 
-- Routing: the FP32 logits are compared bit for bit (both sides form them with one fused
-  multiply-add per term in k order); the chosen experts, the grouping (offsets, rows,
-  row_of) bit for bit; the gates to one FP32 ulp (double affinities on both sides, the
-  exponential from different libraries).
+- Routing.  The oracle forms the affinity logits in double (exact products, a double sum),
+  independent of any GPU summation order; the kernel forms them in FP32 with one fused
+  multiply-add per term in increasing k.  The device logits must lie within the FP32
+  error bound of that summation (u * sum_k |s_k| over the exact prefix sums s_k, u = 2^-24)
+  of the exact ones, and every logit within the order-free bound gamma_D * sum |u c|.
+  Through the sigmoid (slope <= 1/4) that bounds each selection key.  A token whose
+  chosen experts' keys clear its other experts' keys by more than these bounds has one
+  correct selection: the device's must equal the oracle's.  For the few others (counted
+  and reported) the device's selection must be a valid top-k within the bounds.  The
+  grouping (offsets, rows, row_of) must be the oracle's grouping of the device's
+  selection, bit for bit; the gates the oracle's gates of that selection, within the
+  propagated logit bound plus two FP32 ulps.
 - Gather + quantise: bit-exact.
 - Up projection with fused SwiGLU + 1x128 quantisation: the oracle forms h in double from
   its own FP32 GEMM results, the kernel in FP32 from the tensor-core partials, so h differs
   in its last bits.  Scales agree to 1e-5 relative; a code may differ only where h / s lies
   next to a rounding boundary: by one step, in at most 1e-3 of the codes.
-- Down projection and combine: the GEMM tolerance (tests/gpu_util.py).
+- Down projection and combine: the GEMM tolerance (tests/gpu_util.py); the oracle chain
+  runs on the device's (validated) routing.
 Sizes: small ragged configurations checked in full, and the 4096-token, 256-expert layer
 of workload 3 with the routing checked in full and the chain on sampled tokens.
 """
@@ -43,31 +52,92 @@ def _cent_t(cent):
     return torch.from_numpy(np.ascontiguousarray(cent.T)).cuda()
 
 
-def _key_margin(logits, bias, k):
-    """Gap between the k-th and (k+1)-th selection key per token (double)."""
-    key = 1.0 / (1.0 + np.exp(-logits.astype(np.float64))) + bias.astype(np.float64)[None, :]
-    part = -np.sort(-key, axis=1)
-    return part[:, k - 1] - part[:, k] if key.shape[1] > k else np.full(key.shape[0], np.inf)
+U32 = 2.0 ** -24
 
 
-def _check_route(fb, orc, x, cent, bias, k):
+def _apriori_bound(x, cent):
+    """|FP32 dot product - exact| for any summation order: gamma_D * sum_k |u_k c_k|."""
+    u = synth.bf16_to_f32(x).astype(np.float64)
+    D = u.shape[1]
+    return D * U32 / (1 - D * U32) * (np.abs(u) @ np.abs(cent.astype(np.float64)).T)
+
+
+def _sequential_bound(x, cent, pairs):
+    """|FP32 sum - exact| of a chain of fused multiply-adds in increasing k: at most
+    u * sum_k |s_k| over the partial sums, taken here as the exact prefix sums s_k with
+    a relative allowance of 2^-20 for their own rounding.  pairs: (t, e) index arrays."""
+    ts, es = pairs
+    out = np.empty(ts.size)
+    u = synth.bf16_to_f32(x).astype(np.float64)
+    c = cent.astype(np.float64)
+    for i in range(0, ts.size, 256):
+        p = u[ts[i:i + 256]] * c[es[i:i + 256]]
+        np.cumsum(p, axis=1, out=p)
+        out[i:i + 256] = U32 * (1 + 2.0 ** -20) * np.abs(p).sum(axis=1)
+    return out
+
+
+def _decided(key, delta, k):
+    """Tokens whose top-k by `key` stays the top-k for every key within +-delta."""
+    if key.shape[1] <= k:
+        return np.ones(key.shape[0], bool)
+    idx = np.argsort(-key, axis=1, kind="stable")
+    lo = np.take_along_axis(key - delta, idx[:, :k], 1).min(axis=1)
+    hi = np.take_along_axis(key + delta, idx[:, k:], 1).max(axis=1)
+    return lo > hi
+
+
+def _check_route(fb, orc, x, cent, bias, k, r=None):
+    """Check a device routing (run here unless given) against the oracle; return the
+    oracle's view of it: (exact logits, selection, gates, offsets, token_of_row, row_of),
+    the last four being the oracle's grouping and gates of the device's selection."""
     T, E = x.shape[0], cent.shape[0]
-    r = fb.moe_route(dev(x), _cent_t(cent), torch.from_numpy(bias).cuda(), k)
-    torch.cuda.synchronize()
+    if r is None:
+        r = fb.moe_route(dev(x), _cent_t(cent), torch.from_numpy(bias).cuda(), k)
+        torch.cuda.synchronize()
     ol = orc.route_logits(x, cent)
-    assert np.array_equal(r["logits"].cpu().numpy().view(np.uint32), ol.view(np.uint32)), "logits differ"
-    # the decision is well conditioned for every token of these seeds
-    assert np.all(_key_margin(ol, bias, k) > 1e-12)
-    osel, ogate = orc.route_select(ol, bias, k)
-    assert np.array_equal(r["expert_idx"].cpu().numpy(), osel)
-    g = r["gate"].cpu().numpy()
-    ulp = np.abs(g.view(np.int32).astype(np.int64) - ogate.view(np.int32).astype(np.int64))
-    assert ulp.max() <= 1, f"gates differ by {ulp.max()} ulp"
-    offs, tor, row_of = orc.route_permute(osel, E)
+    gl = r["logits"].cpu().numpy().astype(np.float64)
+    bound = _apriori_bound(x, cent)
+    assert np.all(np.abs(gl - ol) <= bound), "logits outside the order-free FP32 bound"
+    key = 1.0 / (1.0 + np.exp(-ol)) + bias.astype(np.float64)[None, :]
+    delta = bound / 4  # the sigmoid's slope is at most 1/4
+    decided = _decided(key, delta, k)
+    if not decided.all():
+        # tighten the bound of the experts that keep a token undecided
+        und = np.nonzero(~decided)[0]
+        idx = np.argsort(-key[und], axis=1, kind="stable")
+        lo = np.take_along_axis(key[und] - delta[und], idx[:, :k], 1).min(axis=1)
+        hi = np.take_along_axis(key[und] + delta[und], idx[:, k:], 1).max(axis=1)
+        near = (key[und] - delta[und] <= hi[:, None]) & (key[und] + delta[und] >= lo[:, None])
+        ti, ei = np.nonzero(near)
+        tb = _sequential_bound(x, cent, (und[ti], ei))
+        assert np.all(np.abs(gl[und[ti], ei] - ol[und[ti], ei]) <= tb), "logits outside the sequential FP32 bound"
+        delta[und[ti], ei] = tb / 4
+        decided = _decided(key, delta, k)
+    gsel = r["expert_idx"].cpu().numpy()
+    osel, _ = orc.route_select(ol, bias, k)
+    assert np.array_equal(gsel[decided], osel[decided]), "a decided token's selection differs"
+    excluded = np.nonzero(~decided)[0]
+    for t in excluded:
+        ch = gsel[t]
+        assert len(set(ch.tolist())) == k and np.all(np.diff(ch) > 0)
+        rest = np.setdiff1d(np.arange(E), ch)
+        assert (key[t, ch] + delta[t, ch]).min() >= (key[t, rest] - delta[t, rest]).max(), \
+            f"token {t}: not a top-{k} within the bounds"
+    print(f"routing: {excluded.size} of {T} tokens within the FP32 bounds of a near-tie "
+          f"(selection checked for validity only)")
+    assert excluded.size <= max(2, T // 256)
+    ogate = orc.route_gates(ol, gsel)
+    g = r["gate"].cpu().numpy().astype(np.float64)
+    s = np.take_along_axis(1.0 / (1.0 + np.exp(-ol)), gsel.astype(np.int64), 1)
+    dmax = np.take_along_axis(delta, gsel.astype(np.int64), 1).max(axis=1, keepdims=True)
+    gbound = dmax * (1 + k) / s.sum(axis=1, keepdims=True) + 2 * U32
+    assert np.all(np.abs(g - ogate) <= gbound), "gates outside the propagated bound"
+    offs, tor, row_of = orc.route_permute(gsel, E)
     assert np.array_equal(r["offsets"].cpu().numpy(), offs)
     assert np.array_equal(r["token_of_row"].cpu().numpy(), tor)
     assert np.array_equal(r["row_of"].cpu().numpy(), row_of)
-    return r, (ol, osel, ogate, offs, tor, row_of)
+    return r, (ol, gsel, ogate, offs, tor, row_of)
 
 
 @pytest.mark.parametrize("T,D,E,k", [(300, 512, 40, 6), (64, 256, 64, 1), (129, 128, 300, 16), (1, 32, 8, 8)])
@@ -172,10 +242,7 @@ def test_chain_small(fb, orc):
     qwd, swd = _quant_experts(fb, wd)
     r, h, sh, Y, out = _gpu_chain(fb, dev(x), _cent_t(cent), torch.from_numpy(bias).cuda(), k,
                                   qwu, swu, qwd, swd)
-    ol = orc.route_logits(x, cent)
-    osel, ogate = orc.route_select(ol, bias, k)
-    offs, tor, row_of = orc.route_permute(osel, E)
-    assert np.array_equal(r["offsets"].cpu().numpy(), offs) and np.array_equal(r["row_of"].cpu().numpy(), row_of)
+    _, (ol, osel, ogate, offs, tor, row_of) = _check_route(fb, orc, x, cent, bias, k, r=r)
     oqa, osa = orc.quant_1x128_rows(x[tor])
     ou = [orc.quant_128x128(wu[e]) for e in range(E)]
     od = [orc.quant_128x128(wd[e]) for e in range(E)]
@@ -206,15 +273,7 @@ def test_chain_full_layer_sampled_tokens(fb, orc):
         del wu, wd
     r, h, sh, Y, out = _gpu_chain(fb, dev(tok), _cent_t(cent), torch.from_numpy(bias).cuda(), k,
                                   qwu, swu, qwd, swd)
-    ol = orc.route_logits(tok, cent)
-    assert np.all(_key_margin(ol, bias, k) > 1e-12)
-    osel, ogate = orc.route_select(ol, bias, k)
-    offs, tor, row_of = orc.route_permute(osel, E)
-    assert np.array_equal(r["logits"].cpu().numpy().view(np.uint32), ol.view(np.uint32))
-    assert np.array_equal(r["expert_idx"].cpu().numpy(), osel)
-    assert np.array_equal(r["offsets"].cpu().numpy(), offs)
-    assert np.array_equal(r["token_of_row"].cpu().numpy(), tor)
-    assert np.array_equal(r["row_of"].cpu().numpy(), row_of)
+    _, (ol, osel, ogate, offs, tor, row_of) = _check_route(fb, orc, tok, cent, bias, k, r=r)
     toks = np.array([0, 1234, 2048, 4095])
     rows = row_of[toks].reshape(-1)
     oqa, osa = orc.quant_1x128_rows(tok[tor[rows]])

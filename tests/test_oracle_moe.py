@@ -1,9 +1,9 @@
 """Pins of the oracle's MoE chain (V3 report §2 DeepSeekMoE, §4 aux-loss-free routing):
-routing logits, top-k selection, grouping, SwiGLU + 1x128 quantisation, combine.
+routing logits, top-k selection and gates, grouping, SwiGLU + 1x128 quantisation, combine.
 
-Each is checked against something other than itself: exact double arithmetic with an
-error bound, exactly representable cases, a brute-force ranking in numpy, the grouping
-invariants, and closed forms of SwiGLU."""
+Each is checked against something other than itself: the exact rational value of the
+logits with an error bound, numpy's double product, exactly representable cases, a
+brute-force ranking in numpy, the grouping invariants, and closed forms of SwiGLU."""
 import numpy as np
 import torch
 
@@ -14,18 +14,36 @@ def _bf16(x):
     return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
 
-def test_route_logits_within_fp32_bound_of_exact(orc):
+def test_route_logits_match_exact_rational_sum(orc):
+    """The double logits against the exact value of the dot product (Python
+    fractions over the exact BF16 and FP32 inputs): within D * 2^-53 * sum|u c|."""
+    from fractions import Fraction
     rng = np.random.default_rng(1)
+    T, D, E = 3, 96, 5
+    xb = _bf16(rng.standard_normal((T, D)))
+    c = (rng.standard_normal((E, D)) / np.sqrt(D)).astype(np.float32)
+    l = orc.route_logits(xb, c)
+    assert l.dtype == np.float64
+    u = synth.bf16_to_f32(xb)
+    for t in range(T):
+        for e in range(E):
+            exact = sum(Fraction(float(u[t, k])) * Fraction(float(c[e, k])) for k in range(D))
+            mag = sum(abs(float(u[t, k]) * float(c[e, k])) for k in range(D))
+            assert abs(Fraction(float(l[t, e])) - exact) <= Fraction(D * mag) * Fraction(2) ** -53
+
+
+def test_route_logits_against_numpy_double_product(orc):
+    rng = np.random.default_rng(11)
     T, D, E = 24, 700, 40
     xb = _bf16(rng.standard_normal((T, D)))
     c = (rng.standard_normal((E, D)) / np.sqrt(D)).astype(np.float32)
-    l = orc.route_logits(xb, c).astype(np.float64)
+    l = orc.route_logits(xb, c)
     u = synth.bf16_to_f32(xb).astype(np.float64)
-    exact = u @ c.astype(np.float64).T
-    bound = D * 2.0 ** -24 * (np.abs(u) @ np.abs(c.astype(np.float64)).T)
-    assert np.all(np.abs(l - exact) <= bound)
+    ref = u @ c.astype(np.float64).T
+    bound = 2 * D * 2.0 ** -53 * (np.abs(u) @ np.abs(c.astype(np.float64)).T)
+    assert np.all(np.abs(l - ref) <= bound)
     # a transposed or shifted operand would be far off
-    assert np.max(np.abs(l - exact)) < 1e-4
+    assert not np.allclose(l[:, 1:], ref[:, :-1], atol=1e-3)
 
 
 def test_route_logits_exact_when_every_partial_sum_is_representable(orc):
@@ -34,17 +52,17 @@ def test_route_logits_exact_when_every_partial_sum_is_representable(orc):
     u = rng.integers(-8, 9, (T, D)).astype(np.float32)      # small integers: exact in BF16
     c = (rng.integers(-16, 17, (E, D)) / 64.0).astype(np.float32)
     l = orc.route_logits(_bf16(u), c)
-    exact = u.astype(np.float64) @ c.astype(np.float64).T     # |partial sums| < 2^24 / 64
-    assert np.array_equal(l.astype(np.float64), exact)
+    exact = u.astype(np.float64) @ c.astype(np.float64).T     # every partial sum exact in double
+    assert np.array_equal(l, exact)
 
 
 def test_route_select_matches_brute_force_ranking(orc):
     rng = np.random.default_rng(3)
     T, E, k = 64, 32, 5
-    l = rng.standard_normal((T, E)).astype(np.float32)
+    l = rng.standard_normal((T, E))
     b = (rng.standard_normal(E) * 0.5).astype(np.float32)
     sel, gate = orc.route_select(l, b, k)
-    s = 1.0 / (1.0 + np.exp(-l.astype(np.float64)))
+    s = 1.0 / (1.0 + np.exp(-l))
     key = s + b.astype(np.float64)
     for t in range(T):
         order = np.argsort(-key[t], kind="stable")[:k]      # stable: lower index first on ties
@@ -52,10 +70,15 @@ def test_route_select_matches_brute_force_ranking(orc):
         ch = np.sort(order)
         assert np.array_equal(gate[t], (s[t, ch] / s[t, ch].sum()).astype(np.float32))
     assert np.allclose(gate.sum(axis=1), 1.0, atol=1e-6)
+    # the gates of a given selection follow the same rule
+    assert np.array_equal(orc.route_gates(l, sel), gate)
+    other = np.sort(np.stack([rng.choice(E, k, replace=False) for _ in range(T)]), axis=1).astype(np.int32)
+    s_o = np.take_along_axis(s, other, axis=1)
+    assert np.array_equal(orc.route_gates(l, other), (s_o / s_o.sum(axis=1, keepdims=True)).astype(np.float32))
 
 
 def test_route_select_ties_go_to_the_lower_index(orc):
-    l = np.zeros((2, 6), np.float32)
+    l = np.zeros((2, 6))
     b = np.array([0.1, 0.3, 0.3, 0.3, 0.0, 0.3], np.float32)
     sel, gate = orc.route_select(l, b, 2)
     assert sel.tolist() == [[1, 2], [1, 2]]
