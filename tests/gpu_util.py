@@ -56,3 +56,26 @@ def sample_rows(M: int, n: int, seed: int, must=()):
     rows = set(int(r) for r in must if 0 <= r < M)
     rows.update(int(r) for r in rng.choice(M, size=min(n, M), replace=False))
     return np.array(sorted(rows), dtype=np.int64)
+
+
+GUARD_ROWS = 3
+
+
+def canary_output(M: int, N: int, dtype, device="cuda"):
+    """An output view C [M, N] inside a NaN-filled buffer with a padded row
+    pitch and guard rows above and below.  Returns (C, buf, rows, cols): the
+    GEMM must write exactly buf[rows, cols] and nothing else."""
+    esize = 2 if dtype == torch.bfloat16 else 4
+    per16 = 16 // esize
+    ld = (N + per16 - 1) // per16 * per16 + 2 * per16  # padded pitch, still a multiple of 16 bytes
+    buf = torch.full((M + 2 * GUARD_ROWS, ld), float("nan"), dtype=dtype, device=device)
+    C = buf[GUARD_ROWS:GUARD_ROWS + M, :N]
+    return C, buf, slice(GUARD_ROWS, GUARD_ROWS + M), slice(0, N)
+
+
+def assert_canaries_untouched(buf: torch.Tensor, rows: slice, cols: slice, what=""):
+    """Every element of buf outside [rows, cols] still holds the NaN it was filled with."""
+    mask = torch.ones(buf.shape, dtype=torch.bool, device=buf.device)
+    mask[rows, cols] = False
+    outside = buf[mask]
+    assert torch.isnan(outside.float()).all(), f"{what}: the GEMM wrote outside C"

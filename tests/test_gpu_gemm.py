@@ -11,7 +11,8 @@ import pytest
 import torch
 
 import synth
-from tests.gpu_util import assert_gemm_close, dev, host_bits, sample_rows
+from tests.gpu_util import (assert_canaries_untouched, assert_gemm_close, canary_output, dev, host_bits,
+                            sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -33,9 +34,11 @@ def tile_n(request, fb):
 def _dense(fb, orc, a_bits, w_bits, out_dtype=torch.bfloat16, rows=None, what=""):
     qa, sa = fb.quant_1x128(dev(a_bits))
     qb, sb = fb.quant_128x128(dev(w_bits))
-    C = fb.gemm_blockscaled(qa, sa, qb, sb, 0, out_dtype=out_dtype)
+    C, buf, rs, cs = canary_output(a_bits.shape[0], w_bits.shape[0], out_dtype)
+    fb.gemm_blockscaled(qa, sa, qb, sb, 0, C=C)
     torch.cuda.synchronize()
     assert fb.get_device_error() == 0
+    assert_canaries_untouched(buf, rs, cs, what)
     oqa, osa = orc.quant_1x128_rows(a_bits)
     oqb, osb = orc.quant_128x128(w_bits)
     if rows is None:
@@ -80,19 +83,45 @@ def test_mla_full(fb, orc, tile_n):
     _dense(fb, orc, d["A"], d["Wkv"], what="mla kv")
 
 
-def test_ffn_sampled_rows(fb, orc):
+FFN_ROWS = sample_rows(16384, 512, seed=5, must=(0, 127, 128, 255, 256, 16255, 16256, 16383))
+
+
+@pytest.fixture(scope="module")
+def ffn_case(orc):
+    """The FFN inputs and the oracle's BF16 result on 512 seeded rows (computed
+    once for every tile width)."""
     d = synth.ffn()
-    rows = sample_rows(16384, 384, seed=5, must=(0, 127, 128, 16383))
-    _dense(fb, orc, d["A"], d["B"], rows=rows, what="ffn")
+    oqa, osa = orc.quant_1x128_rows(d["A"])
+    oqb, osb = orc.quant_128x128(d["B"])
+    ref = orc.bf16_round(orc.gemm_blockscaled(oqa, osa, oqb, osb, 0, rows=FFN_ROWS))
+    return d, ref
+
+
+def test_ffn_sampled_rows(fb, tile_n, ffn_case):
+    """The full 16384x18432x7168 FFN GEMM at every tile width, checked on 512
+    seeded rows (including the first and last rows of the first, second and
+    last M tiles, and both sides of a 256-row pair-tile boundary)."""
+    d, ref = ffn_case
+    qa, sa = fb.quant_1x128(dev(d["A"]))
+    qb, sb = fb.quant_128x128(dev(d["B"]))
+    C, buf, rs, cs = canary_output(16384, 18432, torch.bfloat16)
+    fb.gemm_blockscaled(qa, sa, qb, sb, 0, C=C)
+    torch.cuda.synchronize()
+    assert fb.get_device_error() == 0
+    assert_canaries_untouched(buf, rs, cs, "ffn")
+    got = host_bits(C[torch.from_numpy(FFN_ROWS).cuda()])
+    assert_gemm_close(got, ref, f"ffn tile_n={tile_n}")
 
 
 def _dgrad(fb, orc, dY, W, rows=None, what=""):
     """dX = dY W: dY quantised 1x128 along its channels, W through the transposed block quantiser."""
     qdy, sdy = fb.quant_1x128(dev(dY))
     _, _, qwt, swt = fb.quant_128x128_t(dev(W), straight=False)
-    C = fb.gemm_blockscaled(qdy, sdy, qwt, swt, 0, out_dtype=torch.bfloat16)
+    C, buf, rs, cs = canary_output(dY.shape[0], W.shape[1], torch.bfloat16)
+    fb.gemm_blockscaled(qdy, sdy, qwt, swt, 0, C=C)
     torch.cuda.synchronize()
     assert fb.get_device_error() == 0
+    assert_canaries_untouched(buf, rs, cs, what)
     oqdy, osdy = orc.quant_1x128_rows(dY)
     _, _, oqwt, oswt = orc.quant_128x128_t(W)
     if rows is None:
@@ -117,9 +146,11 @@ def test_dgrad_full_size_sampled(fb, orc):
 def _wgrad(fb, orc, dY, X, rows=None, what=""):
     qdy, sdy = fb.quant_1x128(dev(dY), along=1)   # [Cout, T], [T/128, Cout]
     qx, sx = fb.quant_1x128(dev(X), along=1)      # [Cin, T],  [T/128, Cin]
-    C = fb.gemm_blockscaled(qdy, sdy, qx, sx, 1, out_dtype=torch.float32)
+    C, buf, rs, cs = canary_output(dY.shape[1], X.shape[1], torch.float32)
+    fb.gemm_blockscaled(qdy, sdy, qx, sx, 1, C=C)
     torch.cuda.synchronize()
     assert fb.get_device_error() == 0
+    assert_canaries_untouched(buf, rs, cs, what)
     oqdy, osdy = orc.quant_1x128_cols(dY)
     oqx, osx = orc.quant_1x128_cols(X)
     if rows is None:
@@ -197,20 +228,31 @@ def test_grouped_256_experts_routed(fb, orc, tile_n):
     _grouped(fb, orc, a, offs.astype(np.int64), w, what="grouped 256")
 
 
+def moe_check_rows(offs, n_total=512, seed=3):
+    """Rows checked in the full-size grouped GEMMs: the first and the last row
+    of every non-empty expert, plus seeded rows up to n_total in all."""
+    sizes = np.diff(offs)
+    must = []
+    for e in np.nonzero(sizes)[0]:
+        must += [int(offs[e]), int(offs[e + 1]) - 1]
+    must = sorted(set(must))
+    rng = np.random.default_rng(seed)
+    rest = np.setdiff1d(np.arange(offs[0], offs[-1]), must)
+    extra = rng.choice(rest, size=max(0, min(rest.size, n_total - len(must))), replace=False)
+    return np.array(sorted(set(must) | set(int(r) for r in extra)), dtype=np.int64)
+
+
 def test_moe_full_size_sampled(fb, orc):
     """Config-3 shapes: 4096 tokens routed top-8 over 256 experts -> 32768 rows;
-    up (N=4096, K=7168) and down (N=7168, K=2048) grouped GEMMs, checked on
-    every row of 12 experts (the largest, the smallest non-empty, and random)."""
+    up (N=4096, K=7168) and down (N=7168, K=2048) grouped GEMMs, checked on the
+    first and last row of every non-empty expert plus seeded rows (512 rows
+    in all), so that every expert's offset into B and its scales is exercised."""
     tok = synth.moe_tokens()
     offs, token_of_row = synth.moe_route(tok)
     offs = offs.astype(np.int64)
-    sizes = np.diff(offs)
-    nonempty = np.nonzero(sizes)[0]
-    rng = np.random.default_rng(3)
-    pick = {int(nonempty[np.argmax(sizes[nonempty])]), int(nonempty[np.argmin(sizes[nonempty])])}
-    pick.update(int(e) for e in rng.choice(nonempty, 10, replace=False))
-    pick = sorted(pick)
-    rows = np.concatenate([np.arange(offs[e], offs[e + 1]) for e in pick])
+    rows = moe_check_rows(offs)
+    expert_of_row = np.searchsorted(offs, rows, side="right") - 1
+    assert len(np.unique(expert_of_row)) == np.count_nonzero(np.diff(offs))
 
     for which, A_bits in (("up", np.ascontiguousarray(tok[token_of_row])), ("down", synth.moe_down_input())):
         G = 256
@@ -230,12 +272,10 @@ def test_moe_full_size_sampled(fb, orc):
         del qb, sb, C
         oqa, osa = orc.quant_1x128_rows(A_bits)
         ref = np.empty((rows.size, N), np.float32)
-        pos = 0
-        for e in pick:
-            r = np.arange(offs[e], offs[e + 1])
-            oqb, osb = orc.quant_128x128(synth.moe_weights(which, e, e + 1)[0])
-            ref[pos:pos + r.size] = orc.gemm_blockscaled(oqa, osa, oqb, osb, 0, rows=r)
-            pos += r.size
+        for e in np.unique(expert_of_row):
+            sel = np.nonzero(expert_of_row == e)[0]
+            oqb, osb = orc.quant_128x128(synth.moe_weights(which, int(e), int(e) + 1)[0])
+            ref[sel] = orc.gemm_blockscaled(oqa, osa, oqb, osb, 0, rows=rows[sel])
         assert_gemm_close(got, orc.bf16_round(ref), f"moe {which}")
 
 
