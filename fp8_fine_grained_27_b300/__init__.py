@@ -8,7 +8,9 @@ of the binding fails.
 from .binding import (  # noqa: F401
     Fp8bsError,
     e4m3_encode,
+    debug_site,
     gemm_blockscaled,
+    gemm_clock,
     gemm_ue8m0,
     get_device_error,
     grouped_gemm_moe,

@@ -13,7 +13,8 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libfp8bs.so")
+# FP8BS_LIBRARY=debug selects the bounds-checked build (libfp8bs_debug.so)
+LIB_PATH = os.path.join(_HERE, "libfp8bs_debug.so" if os.environ.get("FP8BS_LIBRARY") == "debug" else "libfp8bs.so")
 
 OK, EINVAL, EALIGN, EARCH, ECUDA, ETIMEOUT = 0, -1, -2, -3, -4, -5
 
@@ -25,6 +26,7 @@ EXPORTS = (
     "fp8_quant_1x128_gather", "fp8_grouped_gemm_moe_swiglu", "fp8_moe_combine", "fp8bs_e4m3_encode", "fp8bs_status_string",
     "fp8bs_get_device_error",
     "fp8bs_selftest_timeout", "fp8bs_selftest_division", "fp8bs_set_gemm_tile_n", "fp8bs_version",
+    "fp8bs_debug_build", "fp8bs_debug_site", "fp8bs_gemm_clock",
 )
 
 
@@ -42,7 +44,7 @@ def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
-            raise ImportError(f"libfp8bs.so is not built ({LIB_PATH}); run fp8_fine_grained_27_b300/build.py")
+            raise ImportError(f"{os.path.basename(LIB_PATH)} is not built ({LIB_PATH}); run fp8_fine_grained_27_b300/build.py")
         L = ctypes.CDLL(LIB_PATH)
         i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
         L.fp8_quant_1x128.argtypes = [vp, i64, i64, i64, i32, vp, i64, vp, i64, vp]
@@ -70,12 +72,16 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_selftest_timeout.argtypes = [i64, vp]
         L.fp8bs_selftest_division.argtypes = [vp, vp]
         L.fp8bs_set_gemm_tile_n.argtypes = [i32]
+        L.fp8bs_debug_build.argtypes = []
+        L.fp8bs_debug_site.argtypes = [vp]
+        L.fp8bs_gemm_clock.argtypes = [vp, vp, i32, vp]
         L.fp8bs_version.restype = ctypes.c_char_p
         for name in ("fp8_quant_1x128", "fp8_quant_128x128", "fp8_quant_128x128_t", "fp8_quant_1x128_ue8m0",
                      "fp8_quant_128x128_ue8m0", "fp8_quant_act_weight", "fp8_gemm_ue8m0", "fp8_gemm_blockscaled",
                      "fp8_grouped_gemm_moe", "fp8_moe_route", "fp8_moe_route_noalloc", "fp8_quant_1x128_gather",
                      "fp8_grouped_gemm_moe_swiglu", "fp8_moe_combine", "fp8bs_e4m3_encode", "fp8bs_get_device_error",
-                     "fp8bs_selftest_timeout", "fp8bs_selftest_division", "fp8bs_set_gemm_tile_n"):
+                     "fp8bs_selftest_timeout", "fp8bs_selftest_division", "fp8bs_set_gemm_tile_n",
+                     "fp8bs_debug_build", "fp8bs_debug_site", "fp8bs_gemm_clock"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -331,3 +337,19 @@ def selftest_division(stream=None):
 
 def selftest_timeout(timeout_ns: int, stream=None):
     _check("fp8bs_selftest_timeout", lib().fp8bs_selftest_timeout(timeout_ns, _stream(stream)))
+
+
+def debug_site(stream=None) -> int:
+    """First failed bounds check since the last read (0: none; always 0 in the release build)."""
+    rc = lib().fp8bs_debug_site(_stream(stream))
+    if rc < 0:
+        raise Fp8bsError("fp8bs_debug_site", rc)
+    return rc
+
+
+def gemm_clock(reset: bool = False, stream=None):
+    """(mean SM MHz the GEMM kernels ran at, launches counted) since the last reset."""
+    mhz, n = ctypes.c_double(0.0), ctypes.c_longlong(0)
+    _check("fp8bs_gemm_clock", lib().fp8bs_gemm_clock(ctypes.byref(mhz), ctypes.byref(n), 1 if reset else 0,
+                                                     _stream(stream)))
+    return mhz.value, n.value

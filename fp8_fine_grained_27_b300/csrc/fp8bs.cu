@@ -831,6 +831,44 @@ int fp8bs_set_gemm_tile_n(int bn)
     return FP8BS_OK;
 }
 
+int fp8bs_gemm_clock(double *mhz, long long *launches, int reset, void *stream)
+{
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned long long h[3] = {0, 0, 0};
+    const unsigned long long zero[3] = {0, 0, 0};
+    if (cudaMemcpyFromSymbolAsync(h, g_fp8bs_clock, sizeof h, 0, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        (reset && cudaMemcpyToSymbolAsync(g_fp8bs_clock, zero, sizeof zero, 0, cudaMemcpyHostToDevice, st) !=
+                      cudaSuccess) ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return FP8BS_ECUDA;
+    if (mhz)
+        *mhz = h[1] ? 1e3 * static_cast<double>(h[0]) / static_cast<double>(h[1]) : 0.0;
+    if (launches)
+        *launches = static_cast<long long>(h[2]);
+    return FP8BS_OK;
+}
+
+int fp8bs_debug_build(void)
+{
+#ifdef FP8BS_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+int fp8bs_debug_site(void *stream)
+{
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int h = 0;
+    const int zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&h, g_fp8bs_debug_site, sizeof(int), 0, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemcpyToSymbolAsync(g_fp8bs_debug_site, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return FP8BS_ECUDA;
+    return h;
+}
+
 int fp8bs_get_device_error(void *stream)
 {
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -174,6 +174,7 @@ __device__ __forceinline__ Tile tile_of(int t, const Params &p, const int *tile_
         const int e = lo;
         const int base = p.offs[e];
         const int m_e = p.offs[e + 1] - base;
+        dbg_ok(e >= 0 && e < p.G && base >= 0 && m_e > 0 && base + m_e <= p.M, DBG_GEMM_GROUP);
         const int mtiles = (m_e + BM - 1) / BM;
         const int local = t - tile_start[e];
         const int nt = local / mtiles;
@@ -360,6 +361,9 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    KernelClock kclock{0, 0};
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        kclock = kernel_clock_begin();
 
     const int num_kb = p.K / BK;
     int total_tiles;
@@ -407,7 +411,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                 // let copies already issued land before the CTA exits
                 const uint32_t issued = c;
                 for (uint32_t d = (issued > STAGES ? issued - STAGES : 0); d < issued; ++d)
-                    mbar_wait(bar_full + 8 * (d % STAGES), (d / STAGES) & 1, ERR_TIMEOUT_PRODUCER, &s_abort, 100000000ull);
+                    mbar_wait(bar_full + 8 * (d % STAGES), (d / STAGES) & 1, ERR_TIMEOUT_PRODUCER, nullptr, 100000000ull);
             }
         } else if ((warp == 1 || warp == 3) && lane == 0) {
             // -------------------------------------------------------- MMA issuers
@@ -446,7 +450,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                     --d;
                 if (d > 0) {
                     --d;
-                    mbar_wait(bar_tfull + 8 * (d % NTMEM), (d / NTMEM) & 1, ERR_TIMEOUT_MMA, &s_abort, 100000000ull);
+                    mbar_wait(bar_tfull + 8 * (d % NTMEM), (d / NTMEM) & 1, ERR_TIMEOUT_MMA, nullptr, 100000000ull);
                 }
             }
         }
@@ -508,6 +512,8 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                         return static_cast<uint32_t>(col0 + pc * 32);
                 };
                 const uint32_t tbase = tmem_base + t_lane + b * BN;
+                if (!dbg_ok(b * BN + pcol(NP - 1) + 32 <= L::TMEM_COLS, DBG_GEMM_TMEM))
+                    return false;
                 const float sc = sa_v * sb_v;
                 const float scu = SWIGLU ? sa_v * sbu_v : sc;  // up-block scale (SwiGLU)
                 (void)scu;
@@ -603,9 +609,23 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
             // Scales are loaded two chunks ahead into two fixed registers per
             // operand (the chunk loop is unrolled by two), so each load has a
             // whole chunk pair to land and no register copy waits on it.
-            auto ld_sa = [&](int kb) { return kb < num_kb ? __ldg(sa_ptr + static_cast<int64_t>(kb) * p.ldsa) : 0.0f; };
-            auto ld_sb = [&](int kb) { return (BMODE == 0 && kb < num_kb) ? __ldg(sb_ptr + kb) : 0.0f; };
-            auto ld_sbu = [&](int kb) { return (SWIGLU && kb < num_kb) ? __ldg(sbu_ptr + kb) : 0.0f; };
+            auto ld_sa = [&](int kb) {
+                return (kb < num_kb && dbg_ok(m_row >= 0 && m_row < p.M && m_row < p.ldsa, DBG_GEMM_SCALE_A))
+                           ? __ldg(sa_ptr + static_cast<int64_t>(kb) * p.ldsa)
+                           : 0.0f;
+            };
+            // block row nb of B's scales (per expert when grouped): rows of B / 128, rounded up
+            const int sb_rows = (p.b_rows + 127) / 128;
+            auto ld_sb = [&](int kb) {
+                return (BMODE == 0 && kb < num_kb && dbg_ok(nb >= 0 && nb < sb_rows && kb < p.ldsb, DBG_GEMM_SCALE_B))
+                           ? __ldg(sb_ptr + kb)
+                           : 0.0f;
+            };
+            auto ld_sbu = [&](int kb) {
+                return (SWIGLU && kb < num_kb && dbg_ok(nb + p.N / 128 < sb_rows, DBG_GEMM_SCALE_B))
+                           ? __ldg(sbu_ptr + kb)
+                           : 0.0f;
+            };
             float sa0 = ld_sa(0), sb0 = ld_sb(0), sa1 = ld_sa(1), sb1 = ld_sb(1);
             float su0 = ld_sbu(0), su1 = ld_sbu(1);
             int kb = 0;
@@ -663,8 +683,9 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                         w[q4] = e4m3x2(__fdiv_rn(h[0], scale), __fdiv_rn(h[1], scale)) |
                                 (e4m3x2(__fdiv_rn(h[2], scale), __fdiv_rn(h[3], scale)) << 16);
                     }
-                    *reinterpret_cast<uint4 *>(epi + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
+                    if (dbg_ok(lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16) + 16 <= 2048, DBG_GEMM_EPI_SMEM))
+                        *reinterpret_cast<uint4 *>(epi + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
                 }
                 __syncwarp();
                 const int grow0 = tl.m0 + quarter * 32;
@@ -674,12 +695,14 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                     const int r = idx >> 2, j = idx & 3;
                     const uint4 v = *reinterpret_cast<const uint4 *>(epi + r * 64 + ((j ^ ((r >> 1) & 3)) * 16));
                     const int m = grow0 + r;
-                    if (m < tl.m_end)
+                    if (m < tl.m_end && dbg_ok(m < p.M && tl.n0 + grp * 64 + j * 16 + 16 <= p.N && p.N <= p.ldc,
+                                               DBG_GEMM_SWIGLU_STORE))
                         *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.C) + static_cast<int64_t>(m) * p.ldc +
                                                    tl.n0 + grp * 64 + j * 16) = v;
                 }
                 __syncwarp();
-                if (grp == 0 && tl.m0 + row < tl.m_end)
+                if (grp == 0 && tl.m0 + row < tl.m_end &&
+                    dbg_ok(tl.n0 / 128 < p.N / 128 && tl.m0 + row < p.lds_out, DBG_GEMM_SWIGLU_STORE))
                     p.s_out[static_cast<int64_t>(tl.n0 / 128) * p.lds_out + tl.m0 + row] = scale;
                 ++tcount;
             } else {
@@ -704,7 +727,8 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                             v = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
                                            pack_bf16x2(a[6], a[7]));
                         }
-                        *reinterpret_cast<uint4 *>(epi + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)) = v;
+                        if (dbg_ok(lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16) + 16 <= 2048, DBG_GEMM_EPI_SMEM))
+                            *reinterpret_cast<uint4 *>(epi + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)) = v;
                     }
                     __syncwarp();
 #pragma unroll
@@ -714,7 +738,8 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                         const uint4 v = *reinterpret_cast<const uint4 *>(epi + r * 64 + ((j ^ ((r >> 1) & 3)) * 16));
                         const int m = grow0 + r;
                         const int n = tl.n0 + col0 + g * COLS_PER_ROUND + j * ELEMS_PER_CHUNK;
-                        if (m < tl.m_end && n < p.N) {
+                        if (m < tl.m_end && n < p.N &&
+                            dbg_ok(m < p.M && n + ELEMS_PER_CHUNK <= p.N && p.N <= p.ldc, DBG_GEMM_STORE)) {
                             const int64_t off = static_cast<int64_t>(m) * p.ldc + n;
                             if constexpr (OUT_F32)
                                 *reinterpret_cast<uint4 *>(reinterpret_cast<float *>(p.C) + off) = v;
@@ -730,6 +755,8 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        kernel_clock_end(kclock);
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();

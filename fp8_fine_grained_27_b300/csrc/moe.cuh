@@ -11,9 +11,11 @@
 //
 // The routing decision (an integer) is taken from FP32 logits formed with
 // one fused multiply-add per term in increasing k, then a double sigmoid and
-// bias; that order is part of the definition, so the choice is reproducible
-// bit for bit.  A tensor-core dot product would leave the accumulation order
-// open and let near-ties flip.
+// bias.  A fixed order makes the choice reproducible from run to run, and it
+// bounds each logit's distance from the exact product by the FP32 error of a
+// sequential sum, so that only tokens whose key gap is inside that bound can
+// differ from a choice made on exact logits.  A tensor-core dot product would
+// leave the accumulation order open.
 #pragma once
 #include <cstdint>
 
@@ -365,8 +367,10 @@ __global__ void __launch_bounds__(256) route_group_kernel(const int32_t *__restr
         }
         if (slot >= 0) {
             const int r = base + before + __popc(bal & ((1u << lane) - 1u));
-            token_of_row[r] = static_cast<int32_t>(t);
-            row_of[t * topk + slot] = r;
+            if (dbg_ok(r >= 0 && r < T * topk, DBG_MOE_GROUP)) {
+                token_of_row[r] = static_cast<int32_t>(t);
+                row_of[t * topk + slot] = r;
+            }
         }
         base += total;
     }
@@ -397,6 +401,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
             const int32_t r = row_of[t * topk + j];
             if (r < 0 || r >= R)
                 continue;
+            if (!dbg_ok(n + 8 <= ldy, DBG_MOE_COMBINE))
+                continue;
             const float g = gate[t * topk + j];
             const uint4 v = *reinterpret_cast<const uint4 *>(Y + static_cast<int64_t>(r) * ldy + n);
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -410,7 +416,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
 #pragma unroll
         for (int i = 0; i < 4; ++i)  // low half = even column
             asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed[i]) : "f"(acc[2 * i + 1]), "f"(acc[2 * i]));
-        *reinterpret_cast<uint4 *>(out + t * ldo + n) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        if (dbg_ok(n + 8 <= ldo, DBG_MOE_COMBINE))
+            *reinterpret_cast<uint4 *>(out + t * ldo + n) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     }
 }
 

@@ -177,6 +177,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    KernelClock kclock{0, 0};
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        kclock = kernel_clock_begin();
     const int num_kb = p.K / BK;
     const int total_tiles = ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
 
@@ -201,7 +204,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (!ok) {  // let copies already issued land before the CTA exits
                 for (uint32_t d = (c > STAGES ? c - STAGES : 0); d < c; ++d)
-                    mbar_wait(bar_full + 8 * (d % STAGES), (d / STAGES) & 1, ERR_TIMEOUT_PRODUCER, &s_abort, 100000000ull);
+                    mbar_wait(bar_full + 8 * (d % STAGES), (d / STAGES) & 1, ERR_TIMEOUT_PRODUCER, nullptr, 100000000ull);
             }
         }
     } else if (warp == 1) {
@@ -240,7 +243,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             if (!ok && c > 0)  // the last committed chain completes before TMEM is freed
-                mbar_wait(bar_empty + 8 * ((c - 1) % STAGES), ((c - 1) / STAGES) & 1, ERR_TIMEOUT_MMA, &s_abort,
+                mbar_wait(bar_empty + 8 * ((c - 1) % STAGES), ((c - 1) / STAGES) & 1, ERR_TIMEOUT_MMA, nullptr,
                           100000000ull);
         }
     } else if (warp >= 4 && warp < 8) {
@@ -332,8 +335,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             auto stage = [&](const uint32_t *w) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4 *>(epi + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)) =
-                        make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                    if (dbg_ok(lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16) + 16 <= 2048, DBG_MX_EPI_SMEM))
+                        *reinterpret_cast<uint4 *>(epi + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)) =
+                            make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
             };
             auto flush = [&](int n0) {
                 __syncwarp();
@@ -344,7 +348,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint4 v = *reinterpret_cast<const uint4 *>(epi + rr * 64 + ((j ^ ((rr >> 1) & 3)) * 16));
                     const int m = grow0 + rr;
                     const int n = n0 + j * (OUT_F32 ? 4 : 8);
-                    if (m < p.M && n < p.N) {
+                    if (m < p.M && n < p.N && dbg_ok(n + (OUT_F32 ? 4 : 8) <= p.N && p.N <= p.ldc, DBG_MX_STORE)) {
                         const int64_t off = static_cast<int64_t>(m) * p.ldc + n;
                         if constexpr (OUT_F32)
                             *reinterpret_cast<uint4 *>(reinterpret_cast<float *>(p.C) + off) = v;
@@ -402,6 +406,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        kernel_clock_end(kclock);
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();

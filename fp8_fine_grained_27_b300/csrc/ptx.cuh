@@ -69,6 +69,38 @@ __device__ int g_fp8bs_error = 0;
 enum : int { ERR_NONE = 0, ERR_TIMEOUT_PRODUCER = 1, ERR_TIMEOUT_MMA = 2,
              ERR_TIMEOUT_CONSUMER = 3, ERR_TIMEOUT_SELFTEST = 4 };
 
+// Bounds checks of the debug build (compiled with -DFP8BS_DEBUG).  Each
+// global, shared-memory and TMEM access site checks its index against the
+// extent that the kernel's arguments (or its own layout) give it; a failed
+// check records the site's number in g_fp8bs_debug_site (first one wins) and
+// the caller skips the access, so a bad index is reported instead of
+// touching memory.  In the release build dbg_ok is the constant true and the
+// checks compile away.
+__device__ int g_fp8bs_debug_site = 0;
+
+enum : int {
+    DBG_QROWS_LOAD = 1, DBG_QROWS_STORE = 2, DBG_QROWS_SCALE = 3,
+    DBG_QT_LOAD = 4, DBG_QT_SMEM = 5, DBG_QT_STORE = 6, DBG_QT_SCALE = 7,
+    DBG_GEMM_SCALE_A = 8, DBG_GEMM_SCALE_B = 9, DBG_GEMM_TMEM = 10, DBG_GEMM_EPI_SMEM = 11,
+    DBG_GEMM_STORE = 12, DBG_GEMM_GROUP = 13, DBG_GEMM_SWIGLU_STORE = 14,
+    DBG_MX_STORE = 15, DBG_MX_EPI_SMEM = 16, DBG_MOE_GROUP = 17, DBG_MOE_COMBINE = 18,
+};
+
+__device__ __forceinline__ bool dbg_ok(bool in_bounds, int site)
+{
+#ifdef FP8BS_DEBUG
+    if (!in_bounds) {
+        atomicCAS(&g_fp8bs_debug_site, 0, site);
+        return false;
+    }
+    return true;
+#else
+    (void)in_bounds;
+    (void)site;
+    return true;
+#endif
+}
+
 // Bounded wait on an mbarrier phase.  Spins briefly, then checks the global
 // timer.  `abort` is a flag in the CTA's shared memory (zeroed at the CTA's
 // start): after `limit_ns` the wait records `code` in the device error word
@@ -76,7 +108,8 @@ enum : int { ERR_NONE = 0, ERR_TIMEOUT_PRODUCER = 1, ERR_TIMEOUT_MMA = 2,
 // CTA that sees the flag raised returns false at once, so the other roles of
 // a CTA give up together.  The flag belongs to one CTA of one launch, so an
 // error that an earlier launch left in the device error word does not make
-// later launches give up.
+// later launches give up.  A null `abort` (a drain that must run to its own
+// limit) never gives up early and raises nothing.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int code, volatile int *abort,
                                           uint64_t limit_ns = 2000000000ull)
 {
@@ -89,14 +122,44 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int cod
     while (true) {
         if (mbar_try_wait(bar, parity))
             return true;
-        if (*abort != 0)
+        if (abort && *abort != 0)
             return false;
         if (globaltimer_ns() - t0 > limit_ns) {
             atomicCAS(&g_fp8bs_error, 0, code);
-            *abort = 1;
+            if (abort)
+                *abort = 1;
             return false;
         }
     }
+}
+
+// Clock record of the GEMM kernels.  CTA 0 of each launch adds the SM cycles
+// and the nanoseconds from the end of its set-up to its end, and counts the
+// launch, so the host can compute the SM clock the GEMMs actually ran at (the
+// board's sampled clock cannot resolve kernels of a millisecond, and the
+// clock drops under the power cap).  g_fp8bs_clock = {cycles, ns, launches}.
+__device__ unsigned long long g_fp8bs_clock[3];
+
+struct KernelClock {
+    unsigned long long cycles, ns;
+};
+
+__device__ __forceinline__ KernelClock kernel_clock_begin()
+{
+    KernelClock k;
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(k.cycles));
+    k.ns = globaltimer_ns();
+    return k;
+}
+
+__device__ __forceinline__ void kernel_clock_end(const KernelClock &k)
+{
+    unsigned long long c;
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(c));
+    const unsigned long long t = globaltimer_ns();
+    atomicAdd(&g_fp8bs_clock[0], c - k.cycles);
+    atomicAdd(&g_fp8bs_clock[1], t - k.ns);
+    atomicAdd(&g_fp8bs_clock[2], 1ull);
 }
 
 // Programmatic dependent launch.  A kernel launched with programmatic stream

@@ -229,7 +229,11 @@ __device__ __forceinline__ void rows_tile(const RowsArgs &a, int64_t tile, uint3
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                v[rr][i] = ok ? ldg_stream(x + src * ldx + kb * 128 + (j + 4 * i) * 8) : make_uint4(0, 0, 0, 0);
+                v[rr][i] = (ok && dbg_ok(src >= 0 && src < (row_map ? src_rows : M) &&
+                                             kb * 128 + (j + 4 * i) * 8 + 8 <= K && K <= ldx,
+                                         DBG_QROWS_LOAD))
+                               ? ldg_stream(x + src * ldx + kb * 128 + (j + 4 * i) * 8)
+                               : make_uint4(0, 0, 0, 0);
         }
         uint32_t am[2];
 #pragma unroll
@@ -291,12 +295,13 @@ __device__ __forceinline__ void rows_tile(const RowsArgs &a, int64_t tile, uint3
                 }
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                    *reinterpret_cast<uint2 *>(q + m * ldq + kb * 128 + (j + 4 * i) * 8) = c[i];
-                if (!kBlock && j == 0)
+                    if (dbg_ok(kb * 128 + (j + 4 * i) * 8 + 8 <= K && K <= ldq, DBG_QROWS_STORE))
+                        *reinterpret_cast<uint2 *>(q + m * ldq + kb * 128 + (j + 4 * i) * 8) = c[i];
+                if (!kBlock && j == 0 && dbg_ok(kb < nkb && m < lds, DBG_QROWS_SCALE))
                     s[kb * lds + m] = sc[rr];
             }
         }
-        if (kBlock && tid == 0)
+        if (kBlock && tid == 0 && dbg_ok(m0 < M && kb < nkb && kb < lds, DBG_QROWS_SCALE))
             s[(m0 / 128) * lds + kb] = sc[0];
     }
 }
@@ -388,7 +393,9 @@ __global__ void __launch_bounds__(kThreads, 4) quant_t_kernel(const uint16_t *__
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int64_t r = r0 + (g0 + 16 * u) * 4 + i;
-                v[u][i] = (colok && r < R) ? ldg_stream(x + r * ldx + c0 + cg * 8) : make_uint4(0, 0, 0, 0);
+                v[u][i] = (colok && r < R && dbg_ok(c0 + cg * 8 + 8 <= ldx, DBG_QT_LOAD))
+                              ? ldg_stream(x + r * ldx + c0 + cg * 8)
+                              : make_uint4(0, 0, 0, 0);
             }
 
         // magnitude maximum of each column pair over this thread's 8 rows
@@ -428,7 +435,8 @@ __global__ void __launch_bounds__(kThreads, 4) quant_t_kernel(const uint16_t *__
             if (g0 == 0 && colok) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    s[rb * lds + c0 + cg * 8 + j] = sc[j];
+                    if (dbg_ok(rb < nrb && c0 + cg * 8 + j < lds, DBG_QT_SCALE))
+                        s[rb * lds + c0 + cg * 8 + j] = sc[j];
             }
         } else {
             uint32_t a = absmax2(absmax2(m4.x, m4.y), absmax2(m4.z, m4.w));
@@ -447,9 +455,10 @@ __global__ void __launch_bounds__(kThreads, 4) quant_t_kernel(const uint16_t *__
             for (int j = 0; j < 8; ++j)
                 sc[j] = sb;
             if (tid == 0) {
-                if (s)
+                if (s && dbg_ok(cb < lds, DBG_QT_SCALE))
                     s[rb * lds + cb] = sb;
-                st[cb * ldst + rb] = sb;
+                if (dbg_ok(rb < ldst, DBG_QT_SCALE))
+                    st[cb * ldst + rb] = sb;
             }
         }
 
@@ -486,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 4) quant_t_kernel(const uint16_t *__
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int64_t r = r0 + g * 4 + i;
-                    if (r < R)
+                    if (r < R && dbg_ok(c0 + cg * 8 + 8 <= ldq, DBG_QT_STORE))
                         *reinterpret_cast<uint2 *>(q + r * ldq + c0 + cg * 8) = make_uint2(lo[u][i], hi[u][i]);
                 }
             }
@@ -496,7 +505,8 @@ __global__ void __launch_bounds__(kThreads, 4) quant_t_kernel(const uint16_t *__
             const int wsw = g ^ (2 * cg);
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc)
-                qs[(cg * 8 + cc) * 32 + wsw] = cw[cc];
+                if (dbg_ok(wsw >= 0 && wsw < 32, DBG_QT_SMEM))
+                    qs[(cg * 8 + cc) * 32 + wsw] = cw[cc];
         }
         __syncthreads();
 
@@ -506,10 +516,13 @@ __global__ void __launch_bounds__(kThreads, 4) quant_t_kernel(const uint16_t *__
             const int idx = tid + kThreads * i;
             const int c = idx >> 3, ch = idx & 7;
             const int f = 2 * (c >> 3);
-            uint4 w4 = *reinterpret_cast<const uint4 *>(&qs[c * 32 + ((4 * ch) ^ (f & 28))]);
+            const int widx = c * 32 + ((4 * ch) ^ (f & 28));
+            uint4 w4 = dbg_ok(widx >= 0 && widx + 4 <= 128 * 32, DBG_QT_SMEM)
+                           ? *reinterpret_cast<const uint4 *>(&qs[widx])
+                           : make_uint4(0, 0, 0, 0);
             if (f & 2)
                 w4 = make_uint4(w4.z, w4.w, w4.x, w4.y);
-            if (c0 + c < C && r0 + ch * 16 < R)
+            if (c0 + c < C && r0 + ch * 16 < R && dbg_ok(r0 + ch * 16 + 16 <= ldqt, DBG_QT_STORE))
                 *reinterpret_cast<uint4 *>(qt + (c0 + c) * ldqt + r0 + ch * 16) = w4;
         }
     }

@@ -332,6 +332,35 @@ int fp8bs_selftest_division(unsigned long long *counts, void *stream);
  */
 int fp8bs_set_gemm_tile_n(int bn);
 
+/*
+ * fp8bs_gemm_clock -- synchronise `stream` and report the SM clock the GEMM
+ * kernels (fp8_gemm_blockscaled, fp8_grouped_gemm_moe(_swiglu),
+ * fp8_gemm_ue8m0) ran at since the last reset: *mhz = the summed SM cycles
+ * over the summed nanoseconds of one CTA per launch (from the end of its
+ * set-up to its end), *launches = the launches counted.  Either pointer may
+ * be NULL; reset != 0 clears the record after reading it.  Launches that
+ * overlap on the GPU each count their own interval.  FP8BS_ECUDA on a CUDA
+ * error.  No counterpart on the pages: a measurement aid (the clock drops
+ * under the board's power cap, and sampling tools cannot resolve kernels of
+ * a millisecond).
+ */
+int fp8bs_gemm_clock(double *mhz, long long *launches, int reset, void *stream);
+
+/*
+ * fp8bs_debug_build -- 1 if this library was compiled with FP8BS_DEBUG (the
+ * bounds-checked build, libfp8bs_debug.so), else 0.
+ *
+ * fp8bs_debug_site -- synchronise `stream`, read and clear the bounds-check
+ * record of the current device: 0 if no check has failed since the last
+ * read, else the number of the first access site whose index fell outside
+ * its extent (the kernel skipped that access; the site numbers are listed in
+ * the library source beside the checks).  Always 0 in the release build,
+ * which has no checks.  FP8BS_ECUDA on a CUDA error.
+ * No counterpart on the pages: a test aid for the kernels' index arithmetic.
+ */
+int fp8bs_debug_build(void);
+int fp8bs_debug_site(void *stream);
+
 /* Human-readable text for a status code (static storage). */
 const char *fp8bs_status_string(int status);
 
