@@ -328,6 +328,36 @@ def moe_combine(Y_bf16: np.ndarray, row_of: np.ndarray, gate: np.ndarray,
 
 # --- power-of-two (UE8M0) scales --------------------------------------------
 
+def token_shards(T: int, world: int):
+    """Token boundaries of `world` data-parallel ranks: contiguous ranges of whole
+    128-token tiles, rank r holding tiles [floor(r n / world), floor((r+1) n / world))
+    of the n = T / 128 tiles.  Returns [(t0, t1)] per rank."""
+    assert T % 128 == 0 and world >= 1
+    n = T // 128
+    return [(128 * (r * n // world), 128 * ((r + 1) * n // world)) for r in range(world)]
+
+
+def wgrad_dp(dY_bf16: np.ndarray, X_bf16: np.ndarray, world: int, threads: int | None = None):
+    """Data-parallel Wgrad over `world` ranks ([V3-report] §7: ZeRO-1 data parallelism
+    over the batch; §6: the Wgrad GEMM in FP8 with FP32 output).  Each rank's shard of
+    tokens (token_shards) gives dW_r = dY_r^T X_r by the single-rank rule (token-wise
+    1x128 tiles, FP32 promotion every 128 tokens, gemm_blockscaled in row-scale mode);
+    the ranks' partials are then summed in FP32 in rank order:
+    dW = ((dW_0 + dW_1) + dW_2) + ...  Returns (dW f32 [Cout, Cin], [dW_r])."""
+    dY = _c(dY_bf16, np.uint16)
+    X = _c(X_bf16, np.uint16)
+    assert dY.shape[0] == X.shape[0]
+    parts = []
+    for t0, t1 in token_shards(dY.shape[0], world):
+        qd, sd = quant_1x128_cols(dY[t0:t1], threads)
+        qx, sx = quant_1x128_cols(X[t0:t1], threads)
+        parts.append(gemm_blockscaled(qd, sd, qx, sx, 1, threads=threads))
+    acc = parts[0].copy()
+    for part in parts[1:]:
+        acc = np.add(acc, part, dtype=np.float32)
+    return acc, parts
+
+
 def pow2_exponent(amax: float) -> int:
     """e of the tile scale 2^e: the smallest integer with amax <= 448 * 2^e (e >= -127; 0 for amax 0)."""
     return int(lib().orc_pow2_exponent(float(amax)))
