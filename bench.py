@@ -204,13 +204,20 @@ METRIC = "block-scaled FP8 GEMM TFLOPS (% of B300 FP8 peak); quantize GB/s (% HB
 
 def bench_config(args, world):
     """The `config` object of both arms' lines (same keys, same values)."""
+    if world == 1:
+        par = "single GPU"
+    elif args.workload == "wgrad":
+        par = f"data parallel x{world}: each rank's 16384 tokens, FP32 dW partials reduce-scattered"
+    else:
+        par = f"replicas x{world}"
     return {**workload_desc(args.workload),
             "l2": f"flushed ({args.flush_mb} MB {args.flush_mode}) before every step",
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+            "parallelism": par}
 
 
-# kernels one labelled C-ABI call launches (fp8_moe_route: logits, selection, grouping)
-KERNELS_PER_CALL = {"route": 3}
+# kernels of this library one labelled call launches (fp8_moe_route: logits, selection,
+# grouping; the data-parallel reduce-scatter is the collective library's, none of ours)
+KERNELS_PER_CALL = {"route": 3, "reduce_scatter": 0}
 
 
 def gemm_flops(name):
@@ -436,6 +443,13 @@ def run_ours(args, rank, world):
         dist.init_process_group("nccl")
     step = Step(args.workload, fb, torch, seed=rank)
     launches = step.launches()
+    if dist is not None and args.workload == "wgrad":
+        # data-parallel Wgrad: each rank's tokens give an FP32 partial dW; one
+        # reduce-scatter sums them and leaves each rank its rows (ZeRO-1)
+        from fp8_fine_grained_27_b300 import dp
+        dw_rows = torch.empty((step.d["C"][0].shape[0] // world, step.d["C"][0].shape[1]), dtype=torch.float32,
+                              device="cuda")
+        launches.append(("reduce_scatter", lambda: dp.reduce_scatter_rows(step.d["C"][0], out=dw_rows)))
     flush = torch.empty(args.flush_mb << 20, dtype=torch.uint8, device="cuda")
     # A write-only flush leaves L2 full of dirty lines, which the step's first
     # kernel then has to write back to HBM on top of its own traffic; reading a
@@ -481,6 +495,7 @@ def run_ours(args, rank, world):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+    fb.gemm_clock(reset=True)
     t0 = time.time()
     # The timed region: each step's launches go out back to back, as a caller
     # issues them, with events only around the step.
@@ -494,6 +509,9 @@ def run_ours(args, rank, world):
     if dist:
         dist.barrier()
     t1 = time.time()
+    # the SM clock the GEMM kernels ran at in the timed region (measured in the
+    # kernels: the sampled board clock cannot resolve them)
+    gemm_mhz, gemm_launches = fb.gemm_clock(reset=True)
     if fb.get_device_error() != 0:
         raise RuntimeError("device error during the warm-up or the timed region")
     # A second pass over the same number of steps puts events between the
@@ -508,6 +526,7 @@ def run_ours(args, rank, world):
             evk[k][j + 1].record(stream)
     torch.cuda.synchronize()
     t2 = time.time()
+    gemm_mhz_split, _ = fb.gemm_clock(reset=True)
     sampler.stop()
     clocks = sampler.summary(t0, t1)
     clocks_split = sampler.summary(t1, t2)
@@ -566,7 +585,14 @@ def run_ours(args, rank, world):
                      # the power-capped figure, for runs whose clocks show sw_power_cap
                      "peak_sustained": round(fp8_peak_sustained, 1),
                      "frac_sustained": round(achieved / fp8_peak_sustained, 4),
-                     "kernel": "gemm_kernel", "kernel_ms": round(gemm_ms, 5)},
+                     "kernel": "gemm_kernel", "kernel_ms": round(gemm_ms, 5),
+                     # the SM clock inside the GEMM kernels (their own clock64 over
+                     # globaltimer), and the fraction of the peak's cycles the kernel
+                     # keeps busy: achieved x (max clock / that clock) / peak
+                     "sm_mhz_in_kernel": round(gemm_mhz_split, 1) if gemm_mhz_split else None,
+                     "sm_mhz_in_kernel_timed_region": round(gemm_mhz, 1) if gemm_mhz else None,
+                     "frac_at_max_clock": (round(achieved * peaks.get("sm_max_mhz", 2032.0) / gemm_mhz_split / fp8_peak, 4)
+                                           if gemm_mhz_split else None)},
         "quant": {"achieved_gbs": round(quant_gbs, 1), "peak_gbs": peaks["hbm_gbs"],
                   "frac": round(quant_gbs / peaks["hbm_gbs"], 4), "kernel_ms": round(quant_ms, 5),
                   "bytes_per_step": int(qbytes)},
