@@ -122,6 +122,12 @@ struct Markstein2 {
         r2 = pack2(__frcp_rn(s_lo), __frcp_rn(s_hi));
         ns2 = pack2(-s_lo, -s_hi);
     }
+    // with the reciprocals RN(1/s) already formed
+    __device__ __forceinline__ Markstein2(float s_lo, float s_hi, float r_lo, float r_hi)
+    {
+        r2 = pack2(r_lo, r_hi);
+        ns2 = pack2(-s_lo, -s_hi);
+    }
     // quotients of the two values of BF16 pair word w (low half first)
     __device__ __forceinline__ void quot(uint32_t w, float &q_lo, float &q_hi) const
     {
@@ -374,6 +380,9 @@ __global__ void __launch_bounds__(kThreads, 4) quant_t_kernel(const uint16_t *__
 {
     __shared__ __align__(16) uint32_t qs[128 * 32];
     __shared__ __align__(16) uint4 red[kThreads / 32][16];
+    // 1x128 mode: the tile's 128 column scales and their reciprocals, formed once
+    // per tile by warp 0 (every warp needs the same 128)
+    __shared__ __align__(16) float col_s[128], col_r[128];
     grid_launch_dependents();  // a GEMM launched next may set up meanwhile
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -409,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 4) quant_t_kernel(const uint16_t *__
                 m4.z = absmax2(m4.z, v[u][i].z);
                 m4.w = absmax2(m4.w, v[u][i].w);
             }
-        float sc[8];
+        float sc[8], rc[8];
         if constexpr (!kBlock) {
             m4.x = absmax2(m4.x, __shfl_xor_sync(0xFFFFFFFFu, m4.x, 16));
             m4.y = absmax2(m4.y, __shfl_xor_sync(0xFFFFFFFFu, m4.y, 16));
@@ -418,26 +427,40 @@ __global__ void __launch_bounds__(kThreads, 4) quant_t_kernel(const uint16_t *__
             if (lane < 16)
                 red[warp][cg] = m4;
             __syncthreads();
+            if (warp == 0) {
+                // lane l: columns 4l .. 4l+3 (two BF16 pair words of group l/2)
+                const int gq = lane >> 1, hw = lane & 1;
+                const uint4 r0 = red[0][gq];
+                uint32_t ma = hw ? r0.z : r0.x, mb = hw ? r0.w : r0.y;
 #pragma unroll
-            for (int w = 0; w < kThreads / 32; ++w) {
-                const uint4 o = red[w][cg];
-                m4.x = absmax2(m4.x, o.x);
-                m4.y = absmax2(m4.y, o.y);
-                m4.z = absmax2(m4.z, o.z);
-                m4.w = absmax2(m4.w, o.w);
-            }
-            const uint32_t mw[4] = {m4.x & 0x7FFF7FFFu, m4.y & 0x7FFF7FFFu, m4.z & 0x7FFF7FFFu, m4.w & 0x7FFF7FFFu};
+                for (int w = 1; w < kThreads / 32; ++w) {
+                    const uint4 o = red[w][gq];
+                    ma = absmax2(ma, hw ? o.z : o.x);
+                    mb = absmax2(mb, hw ? o.w : o.y);
+                }
+                ma &= 0x7FFF7FFFu;
+                mb &= 0x7FFF7FFFu;
+                const float s4[4] = {tile_scale(__uint_as_float((ma & 0xFFFFu) << 16)),
+                                     tile_scale(__uint_as_float(ma & 0xFFFF0000u)),
+                                     tile_scale(__uint_as_float((mb & 0xFFFFu) << 16)),
+                                     tile_scale(__uint_as_float(mb & 0xFFFF0000u))};
+                *reinterpret_cast<float4 *>(&col_s[4 * lane]) = make_float4(s4[0], s4[1], s4[2], s4[3]);
+                *reinterpret_cast<float4 *>(&col_r[4 * lane]) =
+                    make_float4(__frcp_rn(s4[0]), __frcp_rn(s4[1]), __frcp_rn(s4[2]), __frcp_rn(s4[3]));
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                sc[2 * p] = tile_scale(__uint_as_float((mw[p] & 0xFFFFu) << 16));
-                sc[2 * p + 1] = tile_scale(__uint_as_float(mw[p] & 0xFFFF0000u));
+                for (int j = 0; j < 4; ++j)
+                    if (c0 + 4 * lane + j < C && dbg_ok(rb < nrb && c0 + 4 * lane + j < lds, DBG_QT_SCALE))
+                        s[rb * lds + c0 + 4 * lane + j] = s4[j];
             }
-            if (g0 == 0 && colok) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (dbg_ok(rb < nrb && c0 + cg * 8 + j < lds, DBG_QT_SCALE))
-                        s[rb * lds + c0 + cg * 8 + j] = sc[j];
-            }
+            __syncthreads();
+            const float4 sa4 = *reinterpret_cast<const float4 *>(&col_s[cg * 8]);
+            const float4 sb4 = *reinterpret_cast<const float4 *>(&col_s[cg * 8 + 4]);
+            const float4 ra4 = *reinterpret_cast<const float4 *>(&col_r[cg * 8]);
+            const float4 rb4 = *reinterpret_cast<const float4 *>(&col_r[cg * 8 + 4]);
+            sc[0] = sa4.x, sc[1] = sa4.y, sc[2] = sa4.z, sc[3] = sa4.w;
+            sc[4] = sb4.x, sc[5] = sb4.y, sc[6] = sb4.z, sc[7] = sb4.w;
+            rc[0] = ra4.x, rc[1] = ra4.y, rc[2] = ra4.z, rc[3] = ra4.w;
+            rc[4] = rb4.x, rc[5] = rb4.y, rc[6] = rb4.z, rc[7] = rb4.w;
         } else {
             uint32_t a = absmax2(absmax2(m4.x, m4.y), absmax2(m4.z, m4.w));
 #pragma unroll
@@ -451,9 +474,10 @@ __global__ void __launch_bounds__(kThreads, 4) quant_t_kernel(const uint16_t *__
             for (int w = 1; w < kThreads / 32; ++w)
                 b = absmax2(b, red[w][0].x);
             const float sb = tile_scale(pair_max_to_f32(b));
+            const float rb_ = __frcp_rn(sb);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                sc[j] = sb;
+                sc[j] = sb, rc[j] = rb_;
             if (tid == 0) {
                 if (s && dbg_ok(cb < lds, DBG_QT_SCALE))
                     s[rb * lds + cb] = sb;
@@ -469,7 +493,8 @@ __global__ void __launch_bounds__(kThreads, 4) quant_t_kernel(const uint16_t *__
         for (int j = 1; j < 8; ++j)
             smin = fminf(smin, sc[j]);
         if (markstein_ok(smin)) {
-            const Markstein2 d0(sc[0], sc[1]), d1(sc[2], sc[3]), d2(sc[4], sc[5]), d3(sc[6], sc[7]);
+            const Markstein2 d0(sc[0], sc[1], rc[0], rc[1]), d1(sc[2], sc[3], rc[2], rc[3]),
+                d2(sc[4], sc[5], rc[4], rc[5]), d3(sc[6], sc[7], rc[6], rc[7]);
 #pragma unroll
             for (int u = 0; u < 2; ++u)
 #pragma unroll
