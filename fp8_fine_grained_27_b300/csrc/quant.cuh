@@ -88,19 +88,21 @@ __device__ __forceinline__ uint32_t codes_pow2(uint32_t w, float inv)
 // x / s for the two values of a BF16 pair, by Markstein's division
 // (P. Markstein, "Computation of elementary functions on the IBM RISC
 // System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with r = RN(1/s)
-// taken once per tile, q0 = RN(x r), the remainder e = x - s q0 (one fused
-// multiply-add) and q = RN(q0 + e r) -- three floating-point operations per
-// value, issued two values at a time (f32x2), instead of a full IEEE divide.
-// q can differ from the IEEE quotient in its last bit (near underflow), but
-// its E4M3 code never does: fp8bs_selftest_division encodes both for every
-// BF16 amax and every BF16 x with |x| <= amax (about 2^31 pairs) and finds no
-// difference.  (RN(x r) alone is not enough: its codes differ for about 3e4
-// of those pairs.)  The one value whose sign the correction step loses is
-// x = -0 (q = +0); the callers OR the input sign bits into the codes
-// (signs4), which restores it and changes no other code, since every other
-// quotient already carries x's sign.  The low and high value may have
-// different scales (two columns of the transposed quantiser).  Scales below
-// 2^-100 (reciprocal near overflow) take the IEEE divide instead.
+// taken once per tile, q0 = RN(x r), the remainder t = q0 s - x (one fused
+// multiply-add) and q = RN(q0 - t r) -- four floating-point operations per
+// value pair, issued two values at a time (f32x2), instead of a full IEEE
+// divide.  q can differ from the IEEE quotient in its last bit (near
+// underflow), but its E4M3 code never does: fp8bs_selftest_division encodes
+// both for every BF16 amax and every BF16 x with |x| <= amax (about 2^31
+// pairs) and finds no difference.  (RN(x r) alone is not enough: its codes
+// differ for about 3e4 of those pairs.)  The remainder is taken as q0 s - x,
+// the negative of Markstein's x - q0 s, and subtracted: the same exact value
+// and the same rounding for every nonzero x, and for x = +-0 the quotient
+// keeps x's sign (x - q0 s would be +0 for both zeros and lose it), so the
+// codes carry every input's sign with no further step.  The low and high
+// value may have different scales (two columns of the transposed
+// quantiser).  Scales below 2^-100 (reciprocal near overflow) take the IEEE
+// divide instead.
 __device__ __forceinline__ uint64_t pack2(float lo, float hi)
 {
     uint64_t r;
@@ -116,29 +118,34 @@ __device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi)
 __device__ __forceinline__ bool markstein_ok(float s) { return s >= 0x1p-100f; }
 
 struct Markstein2 {
-    uint64_t r2, ns2;
+    uint64_t r2, nr2, s2;  // RN(1/s), -RN(1/s), s for the low and high value
     __device__ __forceinline__ Markstein2(float s_lo, float s_hi)
     {
-        r2 = pack2(__frcp_rn(s_lo), __frcp_rn(s_hi));
-        ns2 = pack2(-s_lo, -s_hi);
+        const float r_lo = __frcp_rn(s_lo), r_hi = __frcp_rn(s_hi);
+        r2 = pack2(r_lo, r_hi);
+        nr2 = pack2(-r_lo, -r_hi);
+        s2 = pack2(s_lo, s_hi);
     }
     // with the reciprocals RN(1/s) already formed
     __device__ __forceinline__ Markstein2(float s_lo, float s_hi, float r_lo, float r_hi)
     {
         r2 = pack2(r_lo, r_hi);
-        ns2 = pack2(-s_lo, -s_hi);
+        nr2 = pack2(-r_lo, -r_hi);
+        s2 = pack2(s_lo, s_hi);
     }
     // quotients of the two values of BF16 pair word w (low half first)
     __device__ __forceinline__ void quot(uint32_t w, float &q_lo, float &q_hi) const
     {
         const uint64_t x2 = pack2(bf16lo(w), bf16hi(w));
-        uint64_t q0, e, q;
+        const uint64_t m1 = 0xBF800000BF800000ull;  // (-1, -1)
+        uint64_t nx2, q0, t, q;
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(nx2) : "l"(x2), "l"(m1));
         asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(x2), "l"(r2));
-        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(e) : "l"(q0), "l"(ns2), "l"(x2));
-        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(e), "l"(r2), "l"(q0));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(t) : "l"(q0), "l"(s2), "l"(nx2));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(t), "l"(nr2), "l"(q0));
         unpack2(q, q_lo, q_hi);
     }
-    // E4M3 codes of the pair, low value in the low byte (a -0 input gives 0x00)
+    // E4M3 codes of the pair, low value in the low byte (signs of zeros kept)
     __device__ __forceinline__ uint32_t codes(uint32_t w) const
     {
         float lo, hi;
@@ -153,18 +160,8 @@ __device__ __forceinline__ uint32_t codes_ieee(uint32_t w, float s_lo, float s_h
     return e4m3x2(__fdiv_rn(bf16lo(w), s_lo), __fdiv_rn(bf16hi(w), s_hi));
 }
 
-// the sign bits of the four BF16 values of w0 (values 0, 1) and w1 (values
-// 2, 3), at bit 7 of bytes 0 .. 3
-__device__ __forceinline__ uint32_t signs4(uint32_t w0, uint32_t w1)
-{
-    return __byte_perm(w0, w1, 0x7531) & 0x80808080u;
-}
-
-// four codes (bytes 0 .. 3) from two 16-bit code pairs and the input words
-__device__ __forceinline__ uint32_t join4(uint32_t c0, uint32_t c1, uint32_t w0, uint32_t w1)
-{
-    return __byte_perm(c0, c1, 0x5410) | signs4(w0, w1);
-}
+// four codes (bytes 0 .. 3) from two 16-bit code pairs
+__device__ __forceinline__ uint32_t join4(uint32_t c0, uint32_t c1) { return __byte_perm(c0, c1, 0x5410); }
 
 __device__ __forceinline__ uint4 ldg_stream(const void *p)
 {
@@ -287,16 +284,16 @@ __device__ __forceinline__ void rows_tile(const RowsArgs &a, int64_t tile, uint3
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const uint4 &x = v[rr][i];
-                        c[i].x = join4(d.codes(x.x), d.codes(x.y), x.x, x.y);
-                        c[i].y = join4(d.codes(x.z), d.codes(x.w), x.z, x.w);
+                        c[i].x = join4(d.codes(x.x), d.codes(x.y));
+                        c[i].y = join4(d.codes(x.z), d.codes(x.w));
                     }
                 } else {
                     const float sv = sc[rr];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const uint4 &x = v[rr][i];
-                        c[i].x = join4(codes_ieee(x.x, sv, sv), codes_ieee(x.y, sv, sv), x.x, x.y);
-                        c[i].y = join4(codes_ieee(x.z, sv, sv), codes_ieee(x.w, sv, sv), x.z, x.w);
+                        c[i].x = join4(codes_ieee(x.x, sv, sv), codes_ieee(x.y, sv, sv));
+                        c[i].y = join4(codes_ieee(x.z, sv, sv), codes_ieee(x.w, sv, sv));
                     }
                 }
 #pragma unroll
@@ -500,8 +497,8 @@ __global__ void __launch_bounds__(kThreads, 4) quant_t_kernel(const uint16_t *__
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const uint4 &x = v[u][i];
-                    lo[u][i] = join4(d0.codes(x.x), d1.codes(x.y), x.x, x.y);
-                    hi[u][i] = join4(d2.codes(x.z), d3.codes(x.w), x.z, x.w);
+                    lo[u][i] = join4(d0.codes(x.x), d1.codes(x.y));
+                    hi[u][i] = join4(d2.codes(x.z), d3.codes(x.w));
                 }
         } else {
 #pragma unroll
@@ -509,8 +506,8 @@ __global__ void __launch_bounds__(kThreads, 4) quant_t_kernel(const uint16_t *__
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const uint4 &x = v[u][i];
-                    lo[u][i] = join4(codes_ieee(x.x, sc[0], sc[1]), codes_ieee(x.y, sc[2], sc[3]), x.x, x.y);
-                    hi[u][i] = join4(codes_ieee(x.z, sc[4], sc[5]), codes_ieee(x.w, sc[6], sc[7]), x.z, x.w);
+                    lo[u][i] = join4(codes_ieee(x.x, sc[0], sc[1]), codes_ieee(x.y, sc[2], sc[3]));
+                    hi[u][i] = join4(codes_ieee(x.z, sc[4], sc[5]), codes_ieee(x.w, sc[6], sc[7]));
                 }
         }
 #pragma unroll
@@ -553,8 +550,8 @@ __global__ void __launch_bounds__(kThreads, 4) quant_t_kernel(const uint16_t *__
     }
 }
 
-// Exhaustive check of the quantisers' division (Markstein2 + signs4) against the IEEE divide over the whole
-// BF16 domain of the quantisers: block = one positive finite BF16 amax
+// Exhaustive check of the quantisers' division (Markstein2) against the IEEE
+// divide over the whole BF16 domain of the quantisers: block = one positive finite BF16 amax
 // (0x0001 .. 0x7F7F), threads = every BF16 x with |x| <= amax, both signs
 // (x and -x form one pair word).  counts[0] += values whose E4M3 codes
 // differ, counts[1] += values whose single-precision quotients differ in
@@ -571,8 +568,8 @@ __global__ void selftest_division_kernel(unsigned long long *counts)
         const uint32_t w = xb | ((xb | 0x8000u) << 16);  // low: +x, high: -x
         const float i_lo = __fdiv_rn(bf16lo(w), s), i_hi = __fdiv_rn(bf16hi(w), s);
         const uint32_t icodes = e4m3x2(i_lo, i_hi);
-        // the quantisers' path: Markstein + sign bits, or the IEEE divide
-        const uint32_t codes = (fast ? d.codes(w) : codes_ieee(w, s, s)) | (signs4(w, 0) & 0xFFFFu);
+        // the quantisers' path: Markstein's division, or the IEEE divide
+        const uint32_t codes = fast ? d.codes(w) : codes_ieee(w, s, s);
         if (fast) {
             float q_lo, q_hi;
             d.quot(w, q_lo, q_hi);

@@ -311,8 +311,8 @@ int fp8bs_e4m3_encode(const float *x, uint8_t *q, int64_t n, void *stream);
 /*
  * fp8bs_selftest_division -- the quantisers divide by the tile scale with a
  * per-tile reciprocal and one Markstein correction instead of an IEEE divide.
- * This diagnostic encodes both quotients to E4M3 (the fast one with the
- * quantisers' sign restoration for -0) for every positive finite BF16 amax
+ * This diagnostic encodes both quotients to E4M3 (the fast one exactly as
+ * the quantisers form it, signs of zeros included) for every positive finite BF16 amax
  * and every BF16 x with |x| <= amax (about 2^31 values of each sign) and
  * writes counts[0] = values whose codes differ (0 means the fast path is
  * bit-exact on every BF16 input), counts[1] = values whose FP32 quotients
