@@ -427,8 +427,13 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                     const uint32_t ph = (c / STAGES) & 1;
                     const int b = c % NTMEM;
                     const uint32_t tph = (c / NTMEM) & 1;
-                    if (!mbar_wait(bar_tempty + 8 * b, tph ^ 1, ERR_TIMEOUT_MMA, &s_abort) ||
-                        !mbar_wait(bar_full + 8 * s, ph, ERR_TIMEOUT_MMA, &s_abort)) {
+                    // The operands are normally in place long before the partial
+                    // buffer is free: wait for them first, so that the MMAs go out
+                    // as soon as the promotion releases the buffer (the loop's
+                    // critical path).  Same-box A/B, FFN GEMM at equal clock:
+                    // 2786-2847 -> 3089-3138 TFLOP/s-at-2032-MHz.
+                    if (!mbar_wait(bar_full + 8 * s, ph, ERR_TIMEOUT_MMA, &s_abort) ||
+                        !mbar_wait(bar_tempty + 8 * b, tph ^ 1, ERR_TIMEOUT_MMA, &s_abort)) {
                         ok = false;
                         break;
                     }
