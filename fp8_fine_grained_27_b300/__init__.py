@@ -28,5 +28,6 @@ from .binding import (  # noqa: F401
     quant_128x128_t,
     selftest_division,
     selftest_timeout,
+    set_gemm_split_last_round,
     set_gemm_tile_n,
 )

@@ -25,8 +25,8 @@ EXPORTS = (
     "fp8_grouped_gemm_moe", "fp8_moe_route_workspace_size", "fp8_moe_route", "fp8_moe_route_noalloc",
     "fp8_quant_1x128_gather", "fp8_grouped_gemm_moe_swiglu", "fp8_moe_combine", "fp8bs_e4m3_encode", "fp8bs_status_string",
     "fp8bs_get_device_error",
-    "fp8bs_selftest_timeout", "fp8bs_selftest_division", "fp8bs_set_gemm_tile_n", "fp8bs_version",
-    "fp8bs_debug_build", "fp8bs_debug_site", "fp8bs_gemm_clock",
+    "fp8bs_selftest_timeout", "fp8bs_selftest_division", "fp8bs_set_gemm_tile_n",
+    "fp8bs_set_gemm_split_last_round", "fp8bs_version", "fp8bs_debug_build", "fp8bs_debug_site", "fp8bs_gemm_clock",
 )
 
 
@@ -72,6 +72,7 @@ def lib() -> ctypes.CDLL:
         L.fp8bs_selftest_timeout.argtypes = [i64, vp]
         L.fp8bs_selftest_division.argtypes = [vp, vp]
         L.fp8bs_set_gemm_tile_n.argtypes = [i32]
+        L.fp8bs_set_gemm_split_last_round.argtypes = [i32]
         L.fp8bs_debug_build.argtypes = []
         L.fp8bs_debug_site.argtypes = [vp]
         L.fp8bs_gemm_clock.argtypes = [vp, vp, i32, vp]
@@ -81,7 +82,7 @@ def lib() -> ctypes.CDLL:
                      "fp8_grouped_gemm_moe", "fp8_moe_route", "fp8_moe_route_noalloc", "fp8_quant_1x128_gather",
                      "fp8_grouped_gemm_moe_swiglu", "fp8_moe_combine", "fp8bs_e4m3_encode", "fp8bs_get_device_error",
                      "fp8bs_selftest_timeout", "fp8bs_selftest_division", "fp8bs_set_gemm_tile_n",
-                     "fp8bs_debug_build", "fp8bs_debug_site", "fp8bs_gemm_clock"):
+                     "fp8bs_set_gemm_split_last_round", "fp8bs_debug_build", "fp8bs_debug_site", "fp8bs_gemm_clock"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -237,6 +238,12 @@ def e4m3_encode(x: torch.Tensor, q=None, stream=None):
 def set_gemm_tile_n(bn: int) -> None:
     """GEMM output tile width: 128, 192, 256, or 0 for automatic."""
     _check("fp8bs_set_gemm_tile_n", lib().fp8bs_set_gemm_tile_n(bn))
+
+
+def set_gemm_split_last_round(on: bool) -> None:
+    """FP32-output GEMMs: share the last round's tiles out by K chunks (True,
+    the default; bit-identical results) or run whole tiles only (False)."""
+    _check("fp8bs_set_gemm_split_last_round", lib().fp8bs_set_gemm_split_last_round(1 if on else 0))
 
 
 def get_device_error(stream=None) -> int:

@@ -25,6 +25,14 @@ static __device__ __align__(256) unsigned char g_route_scratch[kRouteScratchByte
 static_assert(kRouteScratchBytes >= ((fp8bs::moe::kMaxExperts * 4 + 255) / 256) * 256,
               "the static routing scratch must hold the workspace of the largest expert count");
 
+// Flags of the GEMM's K-split last round (one per CTA pair that shares a
+// tile): a ring of kSplitRing slot groups of kSplitGroup flags.  Each launch
+// takes the next group and its own flag value, so launches in flight at the
+// same time on different streams do not share flags (unless more than
+// kSplitRing of them are).
+static constexpr int kSplitGroup = 256, kSplitRing = 256;
+static __device__ uint32_t g_split_flags[kSplitGroup * kSplitRing];
+
 namespace fp8bs {
 
 // A barrier nothing completes, waited on with a short bound: exercises the
@@ -60,6 +68,7 @@ struct DeviceInfo {
     unsigned gemm_attr_set = 0;  // bit per GEMM instance: shared-memory attribute applied
     void *route_scratch = nullptr;  // device address of g_route_scratch
     unsigned mx_attr_set = 0;       // bit per block-scaled GEMM instance
+    uint32_t *split_flags = nullptr;  // device address of g_split_flags
 };
 
 std::mutex g_mu;
@@ -208,6 +217,33 @@ int launch_gemm_bn(int bn, int out_dtype, DeviceInfo *d, const CUtensorMap &tA, 
 }
 
 std::atomic<int> g_tile_n{0};  // fp8bs_set_gemm_tile_n: 0 = automatic
+std::atomic<int> g_split_k{1};  // fp8bs_set_gemm_split_last_round
+std::atomic<uint32_t> g_split_epoch{0};
+
+// The K-split last round for a dense GEMM with FP32 output whose tiles leave
+// the last round of the persistent grid partly idle: the tiles from the
+// second-to-last round on are shared out by K chunks (gemm.cuh, "The last
+// round of tiles").  Sets p.sk_first, the launch's flag group and value.
+int plan_split(DeviceInfo *d, gemm::Params &p, int64_t tiles, int grid, int out_dtype)
+{
+    const int64_t first = (tiles / grid - 1) * grid;
+    if (out_dtype != 1 || g_split_k.load(std::memory_order_relaxed) == 0 || tiles <= grid || tiles % grid == 0 ||
+        grid > kSplitGroup || (tiles - first) * (p.K / 128) >= (int64_t(1) << 31))
+        return FP8BS_OK;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!d->split_flags &&
+            cudaGetSymbolAddress(reinterpret_cast<void **>(&d->split_flags), g_split_flags) != cudaSuccess)
+            return FP8BS_ECUDA;
+    }
+    uint32_t e = g_split_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+    if (e == 0)  // a flag value is never 0, the flags' initial value
+        e = g_split_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+    p.sk_first = static_cast<int>(first);
+    p.sk_flags = d->split_flags + static_cast<int64_t>(e % kSplitRing) * kSplitGroup;
+    p.sk_epoch = e;
+    return FP8BS_OK;
+}
 
 template <int BN, bool OUT_F32>
 int launch_mx(DeviceInfo *d, const CUtensorMap &tA, const CUtensorMap &tB, const mx::Params &p, int grid,
@@ -519,6 +555,9 @@ int fp8_gemm_blockscaled(const uint8_t *A, int64_t lda, const float *sa, int64_t
     const int64_t tiles = ((M + 127) / 128) * ((N + BN - 1) / BN);
     const int grid = static_cast<int>(std::min<int64_t>(tiles, d->num_sms));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    rc = plan_split(d, p, tiles, grid, out_dtype);
+    if (rc != FP8BS_OK)
+        return rc;
     if (b_scale_mode == 0)
         return launch_gemm_bn<0, false>(BN, out_dtype, d, tA, tB, tSB, p, grid, st);
     return launch_gemm_bn<1, false>(BN, out_dtype, d, tA, tB, tSB, p, grid, st);
@@ -828,6 +867,14 @@ int fp8bs_set_gemm_tile_n(int bn)
     if (bn != 0 && bn != 128 && bn != 192 && bn != 256)
         return FP8BS_EINVAL;
     g_tile_n.store(bn, std::memory_order_relaxed);
+    return FP8BS_OK;
+}
+
+int fp8bs_set_gemm_split_last_round(int on)
+{
+    if (on != 0 && on != 1)
+        return FP8BS_EINVAL;
+    g_split_k.store(on, std::memory_order_relaxed);
     return FP8BS_OK;
 }
 

@@ -37,6 +37,21 @@
 //   tempty[b] promotion has read buffer b          (one arrival per promotion warp -> MMA)
 //   sbfull/sbempty  per-stage B row scales (row-scale mode only)
 //
+// The last round of tiles (FP32 output).  When the tiles do not fill the
+// last round of the persistent grid (Wgrad: 448 tiles on 148 CTAs is three
+// rounds and four tiles), the tiles from the second-to-last round on are
+// shared out by K chunks instead: CTA b takes the b-th of G equal runs of
+// their chunks, in tile order, so every CTA does the same number of chunks.
+// A tile then falls to at most two CTAs (every run is longer than a tile).
+// Its first K chunks go to the CTA that holds the tile's end of the run
+// order (CTA b+1, which meets the tile first), and that CTA stores its FP32
+// accumulators in C and raises a flag; CTA b, which meets the tile at the
+// end of its run, waits for the flag, takes those accumulators as its
+// starting values and promotes the remaining chunks.  Every output element
+// is promoted chunk by chunk in K order from zero, exactly as in a whole
+// tile, so the result is bit-identical.  The flag holds a per-launch value,
+// in a ring of flag slots that concurrent launches do not share.
+//
 // SwiGLU variant (V3 report §2: SwiGLU experts; §6.1: the down projection
 // takes the 1x128-quantised SwiGLU output): B holds the gate rows [0, N) and
 // the up rows [N, 2N) of the up projection.  A 128 x 256 MMA tile loads gate
@@ -108,7 +123,7 @@ struct Cfg {
     static constexpr int OFF_EPI = OFF_SBROW + STAGES * SBROW_BYTES;
     static constexpr int OFF_XCH = OFF_EPI + EPI_BYTES;
     static constexpr int OFF_BAR = OFF_XCH + XCH_BYTES;
-    static constexpr int NBAR = 4 * STAGES + 2 * NTMEM + 1;  // + the SwiGLU exchange barrier
+    static constexpr int NBAR = 4 * STAGES + 2 * NTMEM + 3;  // + the SwiGLU exchange and two K-split barriers
     static constexpr int OFF_TMEMSLOT = OFF_BAR + NBAR * 8;
     static constexpr int OFF_TILESTART = (OFF_TMEMSLOT + 4 + 15) / 16 * 16;
     static constexpr int BYTES = OFF_TILESTART + TABLE_BYTES;
@@ -134,7 +149,82 @@ struct Params {
     int group_m;         // raster group (dense only; group_m_for(K))
     const int32_t *offs; // grouped: [G+1] row offsets (device)
     int G;
+    int sk_first = 0x7FFFFFFF;  // first tile shared out by K chunks (dense FP32 output); none by default
+    uint32_t *sk_flags = nullptr;  // flag of the tile split between CTA b and b+1: sk_flags[b]
+    uint32_t sk_epoch = 0;         // this launch's flag value (never 0)
 };
+
+// One piece of work of a CTA: tile t, K chunks [kb0, kb1).
+enum : int { ITEM_FULL = 0, ITEM_HEAD = 1, ITEM_TAIL = 2 };
+struct Item {
+    int t, kb0, kb1, mode;
+};
+
+// The K-split run of one CTA (in shared memory, written once at its start):
+// n_rr whole tiles b, b + G, ... below skf, then the chunks [u0, u1) of tiles
+// skf .. total-1, counted from tile skf's first chunk; s0 = the run's first
+// tile boundary.  The host keeps (total - skf) x nk below 2^31.
+struct SplitRun {
+    int n_rr, skf, u0, u1, s0;
+};
+
+__device__ __forceinline__ void split_run_init(SplitRun &r, int b, int G, int total, int sk_first, int nk)
+{
+    const int skf = min(sk_first, total);
+    r.skf = skf;
+    r.n_rr = skf > b ? (skf - b + G - 1) / G : 0;
+    const int64_t U = static_cast<int64_t>(total - skf) * nk;
+    const int64_t u0 = U * b / G, u1 = U * (b + 1) / G;
+    r.u0 = static_cast<int>(u0);
+    r.u1 = static_cast<int>(u1);
+    r.s0 = static_cast<int>((u0 + nk - 1) / nk * nk);
+}
+
+// Piece j of the work of CTA b of G (the same sequence for its producer, MMA
+// and promotion roles); false past the last piece.  Without the K split
+// (SPLIT false) the pieces are the whole tiles b, b + G, ... below total.
+// The run is read from shared memory for every piece, so that the roles keep
+// only j live across their loops.
+template <bool SPLIT>
+__device__ __forceinline__ bool item_of(int j, int b, int G, int total, int nk, const volatile SplitRun *r, Item &it)
+{
+    if constexpr (!SPLIT) {
+        it = Item{b + j * G, 0, nk, ITEM_FULL};
+        return it.t < total;
+    } else {
+        const int n_rr = r->n_rr;
+        if (j < n_rr) {
+            it = Item{b + j * G, 0, nk, ITEM_FULL};
+            return true;
+        }
+        const int k = j - n_rr;
+        const int u0 = r->u0, u1 = r->u1, s0 = r->s0;
+        const int head = u0 < s0 ? 1 : 0;
+        const int start = k < head ? u0 : s0 + (k - head) * nk;
+        const int end = k < head ? min(u1, s0) : min(u1, start + nk);
+        if (start >= u1)
+            return false;
+        const int rel = start / nk;
+        const int lo = rel * nk, hi = lo + nk;
+        const int len = end - start;
+        it.t = r->skf + rel;
+        if (start > lo) {  // the tile's end of the run order: its first len chunks, to hand on
+            it.kb0 = 0;
+            it.kb1 = len;
+            it.mode = ITEM_HEAD;
+        } else if (end < hi) {  // the tile's start of the run order: its last len chunks, to finish
+            it.kb0 = nk - len;
+            it.kb1 = nk;
+            it.mode = ITEM_TAIL;
+        } else {
+            it.kb0 = 0;
+            it.kb1 = nk;
+            it.mode = ITEM_FULL;
+        }
+        dbg_ok(!(start > lo && end < hi), DBG_GEMM_SPLIT);
+        return true;
+    }
+}
 
 struct Tile {
     int m0, m_end, n0, brow0;
@@ -320,13 +410,21 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
     const uint32_t bar_tfull = bar_sbempty + 8 * STAGES;
     const uint32_t bar_tempty = bar_tfull + 8 * NTMEM;
     const uint32_t bar_xch = bar_tempty + 8 * NTMEM;
+    const uint32_t bar_skhead = bar_xch + 8;  // promotion warps' K-split partial stored
+    const uint32_t bar_sktail = bar_xch + 16; // the partial to continue from is in C
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_TMEMSLOT);
     int *tile_start = reinterpret_cast<int *>(smem + L::OFF_TILESTART);
     // raised by the first wait of this CTA that gives up (see mbar_wait)
     __shared__ int s_abort;
+    // K-split instances: this CTA's run of pieces
+    constexpr bool SPLIT_OK = OUT_F32 && !GROUPED && !SWIGLU;
+    __shared__ SplitRun s_run;
 
     if (threadIdx.x == 0) {
         s_abort = 0;
+        if constexpr (SPLIT_OK)
+            split_run_init(s_run, blockIdx.x, gridDim.x, ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN), p.sk_first,
+                           p.K / BK);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
@@ -338,6 +436,8 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
             mbar_init(bar_tempty + 8 * b, L::NPW);
         }
         mbar_init(bar_xch, L::NPW * 32);
+        mbar_init(bar_skhead, L::NPW);
+        mbar_init(bar_sktail, 1);
         fence_barrier_init();
         fence_proxy_async_smem();
     }
@@ -371,6 +471,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
         total_tiles = tile_start[p.G];
     else
         total_tiles = ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
+    const volatile SplitRun *run = &s_run;
 
     if (warp < kFirstPromoWarp) {
         regs_dec<40>();
@@ -378,9 +479,10 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
             // -------------------------------------------------------- TMA producer
             uint32_t c = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-                const Tile tl = tile_of<BN, GROUPED>(t, p, tile_start);
-                for (int kb = 0; kb < num_kb; ++kb, ++c) {
+            Item it;
+            for (int j = 0; ok && item_of<SPLIT_OK>(j, blockIdx.x, gridDim.x, total_tiles, num_kb, run, it); ++j) {
+                const Tile tl = tile_of<BN, GROUPED>(it.t, p, tile_start);
+                for (int kb = it.kb0; kb < it.kb1; ++kb, ++c) {
                     const int s = c % STAGES;
                     const uint32_t ph = (c / STAGES) & 1;
                     if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, ERR_TIMEOUT_PRODUCER, &s_abort)) {
@@ -419,8 +521,9 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
             constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
             uint32_t c = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-                for (int kb = 0; kb < num_kb; ++kb, ++c) {
+            Item it;
+            for (int j = 0; ok && item_of<SPLIT_OK>(j, blockIdx.x, gridDim.x, total_tiles, num_kb, run, it); ++j) {
+                for (int kb = it.kb0; kb < it.kb1; ++kb, ++c) {
                     if ((c & 1u) != mine)
                         continue;
                     const int s = c % STAGES;
@@ -477,8 +580,9 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
         uint32_t tcount = 0;  // tiles finished (SwiGLU exchange phase)
         (void)tcount;
         bool ok = true;
-        for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-            const Tile tl = tile_of<BN, GROUPED>(t, p, tile_start);
+        Item it;
+        for (int j = 0; ok && item_of<SPLIT_OK>(j, blockIdx.x, gridDim.x, total_tiles, num_kb, run, it); ++j) {
+            const Tile tl = tile_of<BN, GROUPED>(it.t, p, tile_start);
             const int m_row = min(tl.m0 + row, p.M - 1);
             const float *sa_ptr = p.sa + m_row;
             // CPW columns starting at a multiple of CPW never straddle a
@@ -494,6 +598,38 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
 #pragma unroll
             for (int j = 0; j < CPW; ++j)
                 acc[j] = 0.0f;
+            if constexpr (SPLIT_OK) {
+                if (it.mode == ITEM_TAIL) {
+                    // continue from the accumulators CTA b+1 stored for this
+                    // tile's first chunks (one thread waits for its flag)
+                    bool got = true;
+                    if (threadIdx.x == kFirstPromoWarp * 32) {
+                        got = flag_wait(p.sk_flags + blockIdx.x, p.sk_epoch, ERR_TIMEOUT_SPLIT, &s_abort);
+                        if (got)
+                            mbar_arrive(bar_sktail);
+                    }
+                    got = mbar_wait(bar_sktail, 0, ERR_TIMEOUT_SPLIT, &s_abort);
+                    if (!__all_sync(0xFFFFFFFFu, got)) {
+                        ok = false;
+                        break;
+                    }
+                    const int m = tl.m0 + row;
+                    if (m < tl.m_end) {
+                        const float *crow = reinterpret_cast<const float *>(p.C) + static_cast<int64_t>(m) * p.ldc;
+#pragma unroll
+                        for (int j = 0; j < CPW; j += 4) {
+                            const int n = tl.n0 + col0 + j;
+                            if (n < p.N && dbg_ok(m < p.M && n + 4 <= p.N && p.N <= p.ldc, DBG_GEMM_SPLIT)) {
+                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(crow + n));
+                                acc[j] = v.x;
+                                acc[j + 1] = v.y;
+                                acc[j + 2] = v.z;
+                                acc[j + 3] = v.w;
+                            }
+                        }
+                    }
+                }
+            }
 
             // One K chunk: wait for its partial, read it from TMEM, release the
             // buffer, fold it into acc with the chunk's scales.
@@ -614,27 +750,28 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
             // Scales are loaded two chunks ahead into two fixed registers per
             // operand (the chunk loop is unrolled by two), so each load has a
             // whole chunk pair to land and no register copy waits on it.
+            const int kend = it.kb1;
             auto ld_sa = [&](int kb) {
-                return (kb < num_kb && dbg_ok(m_row >= 0 && m_row < p.M && m_row < p.ldsa, DBG_GEMM_SCALE_A))
+                return (kb < kend && dbg_ok(m_row >= 0 && m_row < p.M && m_row < p.ldsa, DBG_GEMM_SCALE_A))
                            ? __ldg(sa_ptr + static_cast<int64_t>(kb) * p.ldsa)
                            : 0.0f;
             };
             // block row nb of B's scales (per expert when grouped): rows of B / 128, rounded up
             const int sb_rows = (p.b_rows + 127) / 128;
             auto ld_sb = [&](int kb) {
-                return (BMODE == 0 && kb < num_kb && dbg_ok(nb >= 0 && nb < sb_rows && kb < p.ldsb, DBG_GEMM_SCALE_B))
+                return (BMODE == 0 && kb < kend && dbg_ok(nb >= 0 && nb < sb_rows && kb < p.ldsb, DBG_GEMM_SCALE_B))
                            ? __ldg(sb_ptr + kb)
                            : 0.0f;
             };
             auto ld_sbu = [&](int kb) {
-                return (SWIGLU && kb < num_kb && dbg_ok(nb + p.N / 128 < sb_rows, DBG_GEMM_SCALE_B))
+                return (SWIGLU && kb < kend && dbg_ok(nb + p.N / 128 < sb_rows, DBG_GEMM_SCALE_B))
                            ? __ldg(sbu_ptr + kb)
                            : 0.0f;
             };
-            float sa0 = ld_sa(0), sb0 = ld_sb(0), sa1 = ld_sa(1), sb1 = ld_sb(1);
-            float su0 = ld_sbu(0), su1 = ld_sbu(1);
-            int kb = 0;
-            for (; kb + 1 < num_kb; kb += 2) {
+            int kb = it.kb0;
+            float sa0 = ld_sa(kb), sb0 = ld_sb(kb), sa1 = ld_sa(kb + 1), sb1 = ld_sb(kb + 1);
+            float su0 = ld_sbu(kb), su1 = ld_sbu(kb + 1);
+            for (; kb + 1 < kend; kb += 2) {
                 if (!promote(sa0, sb0, su0)) {
                     ok = false;
                     break;
@@ -650,7 +787,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                 sb1 = ld_sb(kb + 3);
                 su1 = ld_sbu(kb + 3);
             }
-            if (ok && kb < num_kb && !promote(sa0, sb0, su0))
+            if (ok && kb < kend && !promote(sa0, sb0, su0))
                 ok = false;
             if (!ok)
                 break;
@@ -753,6 +890,21 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                         }
                     }
                     __syncwarp();
+                }
+                if constexpr (SPLIT_OK) {
+                    if (it.mode == ITEM_HEAD) {
+                        // the partial is in C: publish it to CTA b-1 once every
+                        // promotion warp's stores are visible at GPU scope
+                        __threadfence();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(bar_skhead);
+                        if (threadIdx.x == kFirstPromoWarp * 32) {
+                            if (mbar_wait(bar_skhead, 0, ERR_TIMEOUT_SPLIT, &s_abort) &&
+                                dbg_ok(blockIdx.x >= 1, DBG_GEMM_SPLIT))
+                                flag_release(p.sk_flags + blockIdx.x - 1, p.sk_epoch);
+                        }
+                    }
                 }
             }
         }

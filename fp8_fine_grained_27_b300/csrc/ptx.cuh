@@ -67,7 +67,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 __device__ int g_fp8bs_error = 0;
 
 enum : int { ERR_NONE = 0, ERR_TIMEOUT_PRODUCER = 1, ERR_TIMEOUT_MMA = 2,
-             ERR_TIMEOUT_CONSUMER = 3, ERR_TIMEOUT_SELFTEST = 4 };
+             ERR_TIMEOUT_CONSUMER = 3, ERR_TIMEOUT_SELFTEST = 4, ERR_TIMEOUT_SPLIT = 5 };
 
 // Bounds checks of the debug build (compiled with -DFP8BS_DEBUG).  Each
 // global, shared-memory and TMEM access site checks its index against the
@@ -83,7 +83,7 @@ enum : int {
     DBG_QT_LOAD = 4, DBG_QT_SMEM = 5, DBG_QT_STORE = 6, DBG_QT_SCALE = 7,
     DBG_GEMM_SCALE_A = 8, DBG_GEMM_SCALE_B = 9, DBG_GEMM_TMEM = 10, DBG_GEMM_EPI_SMEM = 11,
     DBG_GEMM_STORE = 12, DBG_GEMM_GROUP = 13, DBG_GEMM_SWIGLU_STORE = 14,
-    DBG_MX_STORE = 15, DBG_MX_EPI_SMEM = 16, DBG_MOE_GROUP = 17, DBG_MOE_COMBINE = 18,
+    DBG_MX_STORE = 15, DBG_MX_EPI_SMEM = 16, DBG_MOE_GROUP = 17, DBG_MOE_COMBINE = 18, DBG_GEMM_SPLIT = 19,
 };
 
 __device__ __forceinline__ bool dbg_ok(bool in_bounds, int site)
@@ -130,6 +130,41 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int cod
                 *abort = 1;
             return false;
         }
+    }
+}
+
+// A flag in global memory that one CTA sets (release at GPU scope, after its
+// data) and another CTA of the same launch waits for (acquire at GPU scope).
+__device__ __forceinline__ void flag_release(uint32_t *f, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t flag_acquire(const uint32_t *f)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+
+// Bounded wait until *f == v, with the give-up rules of mbar_wait.
+__device__ __forceinline__ bool flag_wait(const uint32_t *f, uint32_t v, int code, volatile int *abort,
+                                          uint64_t limit_ns = 2000000000ull)
+{
+    const uint64_t t0 = globaltimer_ns();
+#pragma unroll 1
+    while (true) {
+        if (flag_acquire(f) == v)
+            return true;
+        if (abort && *abort != 0)
+            return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            atomicCAS(&g_fp8bs_error, 0, code);
+            if (abort)
+                *abort = 1;
+            return false;
+        }
+        __nanosleep(256);
     }
 }
 

@@ -333,6 +333,20 @@ int fp8bs_selftest_division(unsigned long long *counts, void *stream);
 int fp8bs_set_gemm_tile_n(int bn);
 
 /*
+ * fp8bs_set_gemm_split_last_round -- 1 (the default): when fp8_gemm_blockscaled
+ * writes FP32 output and its output tiles leave the last round of the
+ * persistent grid partly idle, the tiles from the second-to-last round on are
+ * shared out by K chunks so that every CTA does the same number of chunks; a
+ * tile shared by two CTAs is promoted by one of them over its first chunks
+ * and by the other over the rest, continuing from the first one's FP32
+ * accumulators (which pass through C), so every output element is still
+ * promoted chunk by chunk in K order and the result is bit-identical to
+ * whole tiles.  0: whole tiles only.  Process-wide; FP8BS_EINVAL for any
+ * other value.  No counterpart on the pages (a scheduling choice).
+ */
+int fp8bs_set_gemm_split_last_round(int on);
+
+/*
  * fp8bs_gemm_clock -- synchronise `stream` and report the SM clock the GEMM
  * kernels (fp8_gemm_blockscaled, fp8_grouped_gemm_moe(_swiglu),
  * fp8_gemm_ue8m0) ran at since the last reset: *mhz = the summed SM cycles

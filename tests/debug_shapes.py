@@ -51,6 +51,20 @@ def main():
         fb.set_gemm_tile_n(0)
         clear(f"dense {M}x{N}x{K}")
 
+    # FP32 output over more tiles than CTAs: the last round shared out by K chunks
+    a = synth.fill_bf16(synth.NORMAL, synth.key(100, 1), (2560 - 40, 384), 1.0)
+    w = synth.fill_bf16(synth.NORMAL, synth.key(102, 1), (2048 - 24, 384), 0.02)
+    qa, sa = fb.quant_1x128(dev(a))
+    qb, sb = fb.quant_128x128(dev(w))
+    for tn in (0, 128):
+        fb.set_gemm_tile_n(tn)
+        C = fb.gemm_blockscaled(qa, sa, qb, sb, 0, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        ref = oracle.gemm_blockscaled(*oracle.quant_1x128_rows(a), *oracle.quant_128x128(w), 0)
+        assert_gemm_close(host_bits(C), ref, f"split last round, tile {tn}")
+    fb.set_gemm_tile_n(0)
+    clear("dense FP32, last round split by K")
+
     # Dgrad (transposed weight quantiser) and Wgrad (token-wise quantiser, per-row scales)
     d = synth.dgrad(T=129, Cout=256, Cin=128)
     qdy, sdy = fb.quant_1x128(dev(d["dY"]))

@@ -178,6 +178,72 @@ def test_wgrad_full_size(fb, orc):
     _wgrad(fb, orc, d["dY"], d["X"], what="wgrad")
 
 
+def _split_vs_whole(fb, run, M, N, what):
+    """run(C) into a canary-guarded FP32 output twice: with the last round of
+    tiles shared out by K chunks (the default) and with whole tiles.  The two
+    results must be bit-identical, and neither may write outside C."""
+    outs = []
+    for split in (True, False):
+        fb.set_gemm_split_last_round(split)
+        try:
+            C, buf, rs, cs = canary_output(M, N, torch.float32)
+            run(C)
+            torch.cuda.synchronize()
+            assert fb.get_device_error() == 0
+            assert_canaries_untouched(buf, rs, cs, f"{what} split={split}")
+            outs.append(C.clone())
+        finally:
+            fb.set_gemm_split_last_round(True)
+    assert torch.equal(outs[0].view(torch.int32), outs[1].view(torch.int32)), f"{what}: split result differs"
+    return outs[0]
+
+
+@pytest.mark.parametrize("bn", [0, 128])
+def test_split_last_round_wgrad_full(fb, bn):
+    """Workload 4 has 448 tiles of 128x256 (896 of 128x128) on 148 CTAs: its
+    last round is shared out by K chunks, and the result must equal the
+    whole-tile result bit for bit."""
+    d = synth.wgrad()
+    qdy, sdy = fb.quant_1x128(dev(d["dY"]), along=1)
+    qx, sx = fb.quant_1x128(dev(d["X"]), along=1)
+    fb.set_gemm_tile_n(bn)
+    try:
+        _split_vs_whole(fb, lambda C: fb.gemm_blockscaled(qdy, sdy, qx, sx, 1, C=C), 2048, 7168, f"wgrad bn={bn}")
+    finally:
+        fb.set_gemm_tile_n(0)
+
+
+@pytest.mark.parametrize("bn", [0, 128])
+@pytest.mark.parametrize("mode", ["row_scales", "block_scales"])
+def test_split_last_round_small(fb, orc, bn, mode):
+    """160 (or 320) tiles and 3 K chunks: every CTA's run crosses tiles, so
+    most tiles are split between two CTAs.  Bit-identical to whole tiles, and
+    every output against the oracle."""
+    if mode == "row_scales":
+        d = synth.wgrad(T=384, Cout=2048, Cin=2560)
+        qa, sa = fb.quant_1x128(dev(d["dY"]), along=1)
+        qb, sb = fb.quant_1x128(dev(d["X"]), along=1)
+        oqa, osa = orc.quant_1x128_cols(d["dY"])
+        oqb, osb = orc.quant_1x128_cols(d["X"])
+        M, N, bmode = 2048, 2560, 1
+    else:
+        a = synth.fill_bf16(synth.OUTLIER, synth.key(100, 0), (2560, 384), 1.0, 0.01, 50.0, k2=synth.key(101, 0))
+        w = synth.fill_bf16(synth.NORMAL, synth.key(102, 0), (2048, 384), 0.02)
+        qa, sa = fb.quant_1x128(dev(a))
+        qb, sb = fb.quant_128x128(dev(w))
+        oqa, osa = orc.quant_1x128_rows(a)
+        oqb, osb = orc.quant_128x128(w)
+        M, N, bmode = 2560, 2048, 0
+    fb.set_gemm_tile_n(bn)
+    try:
+        got = _split_vs_whole(fb, lambda C: fb.gemm_blockscaled(qa, sa, qb, sb, bmode, C=C), M, N,
+                              f"{mode} bn={bn}")
+    finally:
+        fb.set_gemm_tile_n(0)
+    ref = orc.gemm_blockscaled(oqa, osa, oqb, osb, bmode)
+    assert_gemm_close(host_bits(got), ref, f"split {mode} bn={bn}")
+
+
 def _grouped(fb, orc, a_bits, offs, w_bits, rows=None, what=""):
     G, N, K = w_bits.shape
     qa, sa = fb.quant_1x128(dev(a_bits))
