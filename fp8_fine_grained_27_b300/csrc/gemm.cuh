@@ -706,9 +706,15 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                     fold(0, ra);
                     fold(1, rb);
                 } else if constexpr (BMODE == 1) {
-                    // row-scale folds are twice the work: fold the first two
-                    // pieces between the loads so that the last load is issued
-                    // after two folds rather than three
+                    // Row-scale folds are twice the work: fold the first two
+                    // pieces between the loads.  The buffer is freed only after
+                    // the last fold.  Freeing it as soon as the last loads had
+                    // been waited for (before the last two folds) let the next
+                    // chunk's MMAs corrupt this chunk's values in the first 8
+                    // lanes of the last columns, in about one launch in 20 of
+                    // the Wgrad workload (found by repeating it and comparing
+                    // outputs bit for bit); freeing it after the folds never
+                    // did in 2000 launches.
                     tmem_ld32(tbase + pcol(0), ra);
                     tmem_ld32(tbase + pcol(1), rb);
                     tmem_ld_wait_regs2(ra, rb);
@@ -717,9 +723,9 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                     fold(1, rb);
                     tmem_ld32(tbase + pcol(3), rb);
                     tmem_ld_wait_regs2(ra, rb);
-                    release();
                     fold(2, ra);
                     fold(3, rb);
+                    release();
                 } else {
                     // four loads, each overlapped with the fold of the previous one
                     tmem_ld32(tbase + pcol(0), ra);

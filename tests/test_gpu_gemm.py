@@ -244,6 +244,37 @@ def test_split_last_round_small(fb, orc, bn, mode):
     assert_gemm_close(host_bits(got), ref, f"split {mode} bn={bn}")
 
 
+@pytest.mark.parametrize("workload,launches", [("wgrad", 300), ("mla", 300), ("ffn", 40)])
+def test_repeated_launches_are_bit_identical(fb, workload, launches):
+    """The same GEMM launched many times into a NaN-filled output gives the
+    same bits every time.  A race between a partial buffer's release and its
+    reads showed up only this way: a few 8x4 blocks of the Wgrad output were
+    off by one chunk's contribution in about one launch in 20."""
+    if workload == "wgrad":
+        d = synth.wgrad()
+        qa, sa = fb.quant_1x128(dev(d["dY"]), along=1)
+        qb, sb = fb.quant_1x128(dev(d["X"]), along=1)
+        bmode, dtype = 1, torch.float32
+    else:
+        d = synth.mla() if workload == "mla" else synth.ffn()
+        w = np.concatenate([d["Wq"], d["Wkv"]]) if workload == "mla" else d["B"]
+        qa, sa = fb.quant_1x128(dev(d["A"]))
+        qb, sb = fb.quant_128x128(dev(w))
+        bmode, dtype = 0, torch.bfloat16
+    C = torch.empty((qa.shape[0], qb.shape[0]), dtype=dtype, device="cuda")
+    bits = torch.int32 if dtype == torch.float32 else torch.int16
+    first, differ = None, 0
+    for _ in range(launches):
+        C.fill_(float("nan"))
+        fb.gemm_blockscaled(qa, sa, qb, sb, bmode, C=C)
+        if first is None:
+            first = C.view(bits).clone()
+        elif not torch.equal(C.view(bits), first):
+            differ += 1
+    assert fb.get_device_error() == 0
+    assert differ == 0, f"{workload}: {differ} of {launches - 1} launches differ from the first"
+
+
 def _grouped(fb, orc, a_bits, offs, w_bits, rows=None, what=""):
     G, N, K = w_bits.shape
     qa, sa = fb.quant_1x128(dev(a_bits))
