@@ -35,7 +35,8 @@
 //   empty[s]  MMAs reading stage s are complete    (tcgen05.commit -> producer)
 //   tfull[b]  partial in TMEM buffer b is complete (tcgen05.commit -> promotion)
 //   tempty[b] promotion has read buffer b          (one arrival per promotion warp -> MMA)
-//   sbfull/sbempty  per-stage B row scales (row-scale mode only)
+//   sbfull/sbempty  B row scales of a chunk (row-scale mode only), freed by
+//             the promotion when it has folded the chunk
 //
 // The last round of tiles (FP32 output).  When the tiles do not fill the
 // last round of the persistent grid (Wgrad: 448 tiles on 148 CTAs is three
@@ -117,13 +118,17 @@ struct Cfg {
     static constexpr int FIT = (kMaxSmem - FIXED) / STAGE_BYTES;
     static constexpr int STAGES = (FIT < 6 ? FIT : 6) / 2 * 2;
     static_assert(STAGES >= 4 && STAGES % 2 == 0, "pipeline depth");
+    // Row-scale slots.  A ring twice as deep (so that the producer, which
+    // loads a chunk's scales right after its operands, never waits for the
+    // promotion to free one) measured the same.
+    static constexpr int SB_STAGES = STAGES;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SBROW = OFF_B + STAGES * B_BYTES;
-    static constexpr int OFF_EPI = OFF_SBROW + STAGES * SBROW_BYTES;
+    static constexpr int OFF_EPI = OFF_SBROW + SB_STAGES * SBROW_BYTES;
     static constexpr int OFF_XCH = OFF_EPI + EPI_BYTES;
     static constexpr int OFF_BAR = OFF_XCH + XCH_BYTES;
-    static constexpr int NBAR = 4 * STAGES + 2 * NTMEM + 3;  // + the SwiGLU exchange and two K-split barriers
+    static constexpr int NBAR = 2 * STAGES + 2 * SB_STAGES + 2 * NTMEM + 3;  // + SwiGLU exchange, two K-split
     static constexpr int OFF_TMEMSLOT = OFF_BAR + NBAR * 8;
     static constexpr int OFF_TILESTART = (OFF_TMEMSLOT + 4 + 15) / 16 * 16;
     static constexpr int BYTES = OFF_TILESTART + TABLE_BYTES;
@@ -405,9 +410,10 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
 
     const uint32_t bar_full = sbase + L::OFF_BAR;
     const uint32_t bar_empty = bar_full + 8 * STAGES;
+    constexpr int SB_STAGES = L::SB_STAGES;
     const uint32_t bar_sbfull = bar_empty + 8 * STAGES;
-    const uint32_t bar_sbempty = bar_sbfull + 8 * STAGES;
-    const uint32_t bar_tfull = bar_sbempty + 8 * STAGES;
+    const uint32_t bar_sbempty = bar_sbfull + 8 * SB_STAGES;
+    const uint32_t bar_tfull = bar_sbempty + 8 * SB_STAGES;
     const uint32_t bar_tempty = bar_tfull + 8 * NTMEM;
     const uint32_t bar_xch = bar_tempty + 8 * NTMEM;
     const uint32_t bar_skhead = bar_xch + 8;  // promotion warps' K-split partial stored
@@ -428,8 +434,10 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
-            mbar_init(bar_sbfull + 8 * s, 1);
-            mbar_init(bar_sbempty + 8 * s, L::NPW);
+        }
+        for (int q = 0; q < SB_STAGES; ++q) {
+            mbar_init(bar_sbfull + 8 * q, 1);
+            mbar_init(bar_sbempty + 8 * q, L::NPW);
         }
         for (int b = 0; b < NTMEM; ++b) {
             mbar_init(bar_tfull + 8 * b, 1);
@@ -478,6 +486,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
         if (warp == 0 && lane == 0) {
             // -------------------------------------------------------- TMA producer
             uint32_t c = 0;
+            uint32_t ab_issued = 0, sb_issued = 0;  // chunks whose operand / scale loads are in flight or landed
             bool ok = true;
             Item it;
             for (int j = 0; ok && item_of<SPLIT_OK>(j, blockIdx.x, gridDim.x, total_tiles, num_kb, run, it); ++j) {
@@ -489,6 +498,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                         ok = false;
                         break;
                     }
+                    ab_issued = c + 1;
                     mbar_arrive_expect_tx(bar_full + 8 * s, L::A_BYTES + L::B_BYTES);
                     tma_load_2d(sbase + L::OFF_A + s * L::A_BYTES, &tmA, kb * BK, tl.m0, bar_full + 8 * s);
                     if constexpr (SWIGLU) {  // gate block, then up block (128-row boxes)
@@ -499,21 +509,26 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                         tma_load_2d(sbase + L::OFF_B + s * L::B_BYTES, &tmB, kb * BK, tl.brow0, bar_full + 8 * s);
                     }
                     if constexpr (BMODE == 1) {
-                        if (!mbar_wait(bar_sbempty + 8 * s, ph ^ 1, ERR_TIMEOUT_PRODUCER, &s_abort)) {
+                        const int q = c % SB_STAGES;
+                        if (!mbar_wait(bar_sbempty + 8 * q, ((c / SB_STAGES) & 1) ^ 1, ERR_TIMEOUT_PRODUCER,
+                                       &s_abort)) {
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(bar_sbfull + 8 * s, L::SBROW_BYTES);
-                        tma_load_2d(sbase + L::OFF_SBROW + s * L::SBROW_BYTES, &tmSB, tl.n0, kb,
-                                    bar_sbfull + 8 * s);
+                        sb_issued = c + 1;
+                        mbar_arrive_expect_tx(bar_sbfull + 8 * q, L::SBROW_BYTES);
+                        tma_load_2d(sbase + L::OFF_SBROW + q * L::SBROW_BYTES, &tmSB, tl.n0, kb,
+                                    bar_sbfull + 8 * q);
                     }
                 }
             }
             if (!ok) {
                 // let copies already issued land before the CTA exits
-                const uint32_t issued = c;
-                for (uint32_t d = (issued > STAGES ? issued - STAGES : 0); d < issued; ++d)
+                for (uint32_t d = (ab_issued > STAGES ? ab_issued - STAGES : 0); d < ab_issued; ++d)
                     mbar_wait(bar_full + 8 * (d % STAGES), (d / STAGES) & 1, ERR_TIMEOUT_PRODUCER, nullptr, 100000000ull);
+                for (uint32_t d = (sb_issued > SB_STAGES ? sb_issued - SB_STAGES : 0); d < sb_issued; ++d)
+                    mbar_wait(bar_sbfull + 8 * (d % SB_STAGES), (d / SB_STAGES) & 1, ERR_TIMEOUT_PRODUCER, nullptr,
+                              100000000ull);
             }
         } else if ((warp == 1 || warp == 3) && lane == 0) {
             // -------------------------------------------------------- MMA issuers
@@ -641,7 +656,8 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                 // .sync.aligned TMEM loads
                 bool got = mbar_wait(bar_tfull + 8 * b, tph, ERR_TIMEOUT_CONSUMER, &s_abort);
                 if constexpr (BMODE == 1)
-                    got = got && mbar_wait(bar_sbfull + 8 * s, (c / STAGES) & 1, ERR_TIMEOUT_CONSUMER, &s_abort);
+                    got = got && mbar_wait(bar_sbfull + 8 * (c % SB_STAGES), (c / SB_STAGES) & 1, ERR_TIMEOUT_CONSUMER,
+                                           &s_abort);
                 if (!__all_sync(0xFFFFFFFFu, got))
                     return false;
                 tc_fence_after();
@@ -658,7 +674,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                 const float sc = sa_v * sb_v;
                 const float scu = SWIGLU ? sa_v * sbu_v : sc;  // up-block scale (SwiGLU)
                 (void)scu;
-                const float *sbr = sbrow_smem + s * BN + col0;
+                const float *sbr = sbrow_smem + (c % SB_STAGES) * BN + col0;
                 (void)sbr;
 
                 auto fold = [&](int pc, const uint32_t(&cur)[32]) {
@@ -747,7 +763,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                 if constexpr (BMODE == 1) {
                     __syncwarp();
                     if (lane == 0)
-                        mbar_arrive(bar_sbempty + 8 * s);
+                        mbar_arrive(bar_sbempty + 8 * (c % SB_STAGES));
                 }
                 ++c;
                 return true;
