@@ -375,8 +375,8 @@ class Step:
                                                                   C=d["C"][i])))
             return L
         if self.name == "wgrad":
-            return [("quant_1x128_cols", lambda: fb.quant_1x128(d["dY"], along=1, q=d["qdy"], s=d["sdy"])),
-                    ("quant_1x128_cols", lambda: fb.quant_1x128(d["X"], along=1, q=d["qx"], s=d["sx"])),
+            return [("quant_1x128_cols_dY", lambda: fb.quant_1x128(d["dY"], along=1, q=d["qdy"], s=d["sdy"])),
+                    ("quant_1x128_cols_X", lambda: fb.quant_1x128(d["X"], along=1, q=d["qx"], s=d["sx"])),
                     ("gemm", lambda: fb.gemm_blockscaled(d["qdy"], d["sdy"], d["qx"], d["sx"], 1, C=d["C"][0]))]
         if self.name == "dgrad":
             return [("quant_1x128", lambda: fb.quant_1x128(d["dY"], q=d["qdy"], s=d["sdy"])),
