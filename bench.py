@@ -626,41 +626,45 @@ def run_e2e(args, step, torch, fb, launches, flops, world, dist):
     h2d = sum(p.numel() * p.element_size() for _, p in pinned)
     d2h = sum(o.numel() * o.element_size() for o in out_host)
     n = max(3, min(args.e2e_steps, args.steps))
-    # The read-back of step i runs on a side stream while step i+1's inputs
-    # go up on the launch stream (the link is full duplex); step i+1's
-    # launches wait for that read-back before they overwrite the outputs.
+    # The read-back of step i runs on a side stream while step i+1's inputs go
+    # up and its launches run on the launch stream (the link is full duplex).
+    # The outputs alternate between two device buffers, so step i+1 does not
+    # wait for step i's read-back, only for step i-1's, which used the same
+    # buffer.  Every step still uploads its inputs and reads back its result.
     main = torch.cuda.current_stream()
     side = torch.cuda.Stream()
+    out_sets = [outs, [torch.empty_like(o) for o in outs]]
+    read_back = [None, None]  # the last read-back of each output set
 
-    def one_step(read_back_done):
+    def one_step(k):
         for name, p in pinned:
             targets[name].view(torch.int16).copy_(p.view(torch.int16), non_blocking=True)
-        if read_back_done is not None:
-            main.wait_event(read_back_done)
+        if read_back[k % 2] is not None:
+            main.wait_event(read_back[k % 2])
+        step.d["C"] = out_sets[k % 2]
         for _, f in launches:
             f()
         computed = torch.cuda.Event()
         computed.record(main)
         side.wait_event(computed)
         with torch.cuda.stream(side):
-            for o, h in zip(outs, out_host):
+            for o, h in zip(out_sets[k % 2], out_host):
                 h.copy_(o, non_blocking=True)
         done = torch.cuda.Event()
         done.record(side)
-        return done
+        read_back[k % 2] = done
 
-    done = None
-    for _ in range(2):
-        done = one_step(done)
+    for k in range(2):
+        one_step(k)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     t0 = time.perf_counter()
-    done = None
-    for _ in range(n):
-        done = one_step(done)
+    for k in range(n):
+        one_step(k)
     torch.cuda.synchronize()
     dt = max_over_ranks((time.perf_counter() - t0) / n, dist, "cuda")
+    step.d["C"] = outs
     return {"value": round(job_throughput(flops, dt, world) / 1e12, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": n, "ms_per_step": round(dt * 1e3, 4)}
 

@@ -275,6 +275,60 @@ def test_repeated_launches_are_bit_identical(fb, workload, launches):
     assert differ == 0, f"{workload}: {differ} of {launches - 1} launches differ from the first"
 
 
+@pytest.mark.parametrize("kind", ["grouped", "grouped_swiglu", "ue8m0_bf16", "ue8m0_fp32"])
+def test_repeated_launches_are_bit_identical_other_kernels(fb, kind):
+    """The grouped GEMM, the fused SwiGLU grouped GEMM and the UE8M0 GEMM (both
+    output types), each launched 100 times: identical bits every time."""
+    if kind.startswith("grouped"):
+        G, K = 16, 2048
+        sizes = np.array([0, 700, 5, 129, 1100, 0, 257, 64, 900, 1, 380, 0, 2048, 33, 500, 128])
+        offs = torch.from_numpy(np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)).cuda()
+        M = int(sizes.sum())
+        a = synth.fill_bf16(synth.NORMAL, synth.key(110, 0), (M, K), 1.0)
+        N = 2 * 1024 if kind == "grouped_swiglu" else 1536
+        w = synth.fill_bf16(synth.NORMAL, synth.key(111, 0), (G, N, K), 0.02)
+        qa, sa = fb.quant_1x128(dev(a))
+        wd = dev(w)
+        qb = torch.empty((G, N, K), dtype=torch.uint8, device="cuda")
+        sb = torch.empty((G, N // 128, K // 128), dtype=torch.float32, device="cuda")
+        for e in range(G):
+            fb.quant_128x128(wd[e], q=qb[e], s=sb[e])
+        if kind == "grouped":
+            C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            def run():
+                C.fill_(float("nan"))
+                fb.grouped_gemm_moe(qa, sa, qb, sb, offs, C=C)
+                return C.view(torch.int16)
+        else:
+            Q = torch.empty((M, N // 2), dtype=torch.uint8, device="cuda")
+            S = torch.empty((N // 2 // 128, M), dtype=torch.float32, device="cuda")
+            def run():
+                Q.fill_(0xFF)
+                S.fill_(float("nan"))
+                fb.grouped_gemm_moe_swiglu(qa, sa, qb, sb, offs, Q=Q, s=S)
+                return torch.cat([Q.view(torch.int32).flatten(), S.view(torch.int32).flatten()])
+    else:
+        d = synth.mla()
+        qa, sa = fb.quant_1x128_ue8m0(dev(d["A"]))
+        qb, sb = fb.quant_128x128_ue8m0(dev(np.concatenate([d["Wq"], d["Wkv"]])))
+        dtype = torch.bfloat16 if kind == "ue8m0_bf16" else torch.float32
+        C = torch.empty((qa.shape[0], qb.shape[0]), dtype=dtype, device="cuda")
+        bits = torch.int16 if dtype == torch.bfloat16 else torch.int32
+        def run():
+            C.fill_(float("nan"))
+            fb.gemm_ue8m0(qa, sa, qb, sb, C=C)
+            return C.view(bits)
+    first, differ = None, 0
+    for _ in range(100):
+        out = run()
+        if first is None:
+            first = out.clone()
+        elif not torch.equal(out, first):
+            differ += 1
+    assert fb.get_device_error() == 0
+    assert differ == 0, f"{kind}: {differ} of 99 launches differ from the first"
+
+
 def _grouped(fb, orc, a_bits, offs, w_bits, rows=None, what=""):
     G, N, K = w_bits.shape
     qa, sa = fb.quant_1x128(dev(a_bits))
