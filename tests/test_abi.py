@@ -71,6 +71,11 @@ def test_status_strings_and_argument_errors(libpath):
     assert L.fp8_grouped_gemm_moe(vp(16), 128, vp(16), 4, vp(16), vp(16), vp(16), 0, 4, vp(16), 8, 0,
                                   8, 128, None) == b.EINVAL  # G = 0
     assert L.fp8bs_selftest_timeout(0, None) == b.EINVAL
+    # process-wide switches take only their documented values
+    assert L.fp8bs_set_gemm_tile_n(96) == b.EINVAL
+    assert L.fp8bs_set_gemm_split_last_round(2) == b.EINVAL
+    assert L.fp8bs_set_gemm_split_last_round(0) == b.OK
+    assert L.fp8bs_set_gemm_split_last_round(1) == b.OK
     # sizes past the 32-bit tile indexing are refused before any launch
     big = 1 << 31
     assert L.fp8_gemm_blockscaled(vp(16), 128, vp(16), big, vp(16), 128, vp(16), 1, 0, vp(16), 8, 0,
