@@ -373,6 +373,19 @@ __device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[32])
                  : "memory");
 }
 
+// As tmem_ld_wait_regs2, for two 16-register loads.
+__device__ __forceinline__ void tmem_ld_wait_regs16x2(uint32_t (&r)[16], uint32_t (&q)[16])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]), "+r"(q[0]), "+r"(q[1]), "+r"(q[2]), "+r"(q[3]), "+r"(q[4]),
+                   "+r"(q[5]), "+r"(q[6]), "+r"(q[7]), "+r"(q[8]), "+r"(q[9]), "+r"(q[10]), "+r"(q[11]),
+                   "+r"(q[12]), "+r"(q[13]), "+r"(q[14]), "+r"(q[15])
+                 :
+                 : "memory");
+}
+
 // Wait for both outstanding tcgen05.ld of this warp and tie their registers
 // to the wait, so that no use of them is scheduled before it.
 __device__ __forceinline__ void tmem_ld_wait_regs2(uint32_t (&r)[32], uint32_t (&q)[32])
@@ -595,9 +608,191 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
         uint32_t tcount = 0;  // tiles finished (SwiGLU exchange phase)
         (void)tcount;
         bool ok = true;
+
+        // K split: a TAIL piece waits for the flag of CTA b+1's partial (one
+        // thread waits, the others wait on it); a HEAD piece, once its partial
+        // is in C, publishes it to CTA b-1 when every promotion warp's stores
+        // are visible at GPU scope.
+        auto split_tail_wait = [&]() -> bool {
+            bool got = true;
+            if (threadIdx.x == kFirstPromoWarp * 32) {
+                got = flag_wait(p.sk_flags + blockIdx.x, p.sk_epoch, ERR_TIMEOUT_SPLIT, &s_abort);
+                if (got)
+                    mbar_arrive(bar_sktail);
+            }
+            got = mbar_wait(bar_sktail, 0, ERR_TIMEOUT_SPLIT, &s_abort);
+            return __all_sync(0xFFFFFFFFu, got);
+        };
+        auto split_head_publish = [&]() {
+            __threadfence();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar_skhead);
+            if (threadIdx.x == kFirstPromoWarp * 32) {
+                if (mbar_wait(bar_skhead, 0, ERR_TIMEOUT_SPLIT, &s_abort) && dbg_ok(blockIdx.x >= 1, DBG_GEMM_SPLIT))
+                    flag_release(p.sk_flags + blockIdx.x - 1, p.sk_epoch);
+            }
+        };
+        (void)split_tail_wait;
+        (void)split_head_publish;
+
+        // ---------------------------------- per-row scales at 256 columns
+        // The partial is read from TMEM in the 16x256b shape, eight pieces of
+        // 16 registers: a thread holds rows quarter*32 + 8i + lane/4 (i = 0..3)
+        // and the column pairs col0 + 8k + 2(lane%4) (k = 0..15) of its
+        // warpgroup's 128 columns, acc[32i + 2k + e].  It then needs 32 of the
+        // chunk's B scales instead of 128.  With one row and 128 columns per
+        // thread every lane read all 128 as 16-byte shared-memory broadcasts,
+        // about five wavefronts each, and those loads kept the shared-memory
+        // data pipe 59% busy (ncu, Wgrad GEMM) beside the MMAs' operand reads.
+        // Wgrad GEMM 0.404 -> 0.379 ms, bit-identical.  (Pieces of 32
+        // registers spilled and ran slower.)  The buffer is freed after the
+        // last fold: freeing it after the last loads but before the last folds
+        // let the next chunk's MMAs corrupt this chunk's values (in about one
+        // launch in 20 of the Wgrad workload, found by repeating it and
+        // comparing outputs bit for bit; never after the last fold).
+        constexpr bool RS16 = (BMODE == 1 && BN == 256);
+        auto item_rs16 = [&](const Tile &tl, const Item &it) -> bool {
+            const int t4 = lane >> 2, p2 = (lane & 3) * 2;
+            const int rbase = tl.m0 + quarter * 32 + t4;  // rows rbase + 8i
+            float acc[128];
+#pragma unroll
+            for (int j = 0; j < 128; ++j)
+                acc[j] = 0.0f;
+            if constexpr (SPLIT_OK) {
+                if (it.mode == ITEM_TAIL) {
+                    if (!split_tail_wait())
+                        return false;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int m = rbase + 8 * i;
+                        if (m >= tl.m_end)
+                            continue;
+                        const float *crow = reinterpret_cast<const float *>(p.C) + static_cast<int64_t>(m) * p.ldc;
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            const int n = tl.n0 + col0 + 8 * k + p2;
+                            if (n < p.N && dbg_ok(m < p.M && n + 2 <= p.N && p.N <= p.ldc, DBG_GEMM_SPLIT)) {
+                                const float2 v = __ldcg(reinterpret_cast<const float2 *>(crow + n));
+                                acc[32 * i + 2 * k] = v.x;
+                                acc[32 * i + 2 * k + 1] = v.y;
+                            }
+                        }
+                    }
+                }
+            }
+            auto ld_sa4 = [&](int kb, float (&v)[4]) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int m = min(rbase + 8 * i, p.M - 1);
+                    v[i] = (kb < it.kb1 && dbg_ok(m >= 0 && m < p.ldsa, DBG_GEMM_SCALE_A))
+                               ? __ldg(p.sa + static_cast<int64_t>(kb) * p.ldsa + m)
+                               : 0.0f;
+                }
+            };
+            // acc(i, k) += fl32(sa_i * sb_k) * P(i, k), two columns per instruction,
+            // each rounded as the scalar mul and fmaf would be; piece (h, q):
+            // rows 16h + 8ri + lane/4, column pairs k = 4q + j (j = 0..3)
+            auto fold4 = [&](int h, int q, const uint32_t(&r)[16], const float2(&sbp)[4], const uint64_t(&sa2)[4]) {
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    uint64_t sb2;
+                    asm("mov.b64 %0, {%1, %2};" : "=l"(sb2) : "f"(sbp[jj].x), "f"(sbp[jj].y));
+#pragma unroll
+                    for (int ri = 0; ri < 2; ++ri) {
+                        const int i = 2 * h + ri, k = 4 * q + jj;
+                        uint64_t sc2, a2, p2v;
+                        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(sc2) : "l"(sa2[i]), "l"(sb2));
+                        asm("mov.b64 %0, {%1, %2};" : "=l"(a2) : "f"(acc[32 * i + 2 * k]), "f"(acc[32 * i + 2 * k + 1]));
+                        asm("mov.b64 %0, {%1, %2};" : "=l"(p2v) : "r"(r[4 * jj + 2 * ri]), "r"(r[4 * jj + 2 * ri + 1]));
+                        asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a2) : "l"(sc2), "l"(p2v));
+                        asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[32 * i + 2 * k]), "=f"(acc[32 * i + 2 * k + 1]) : "l"(a2));
+                    }
+                }
+            };
+            for (int kb = it.kb0; kb < it.kb1; ++kb) {
+                float sa[4];
+                ld_sa4(kb, sa);
+                const int b = c % NTMEM;
+                const uint32_t tph = (c / NTMEM) & 1;
+                const int s = c % SB_STAGES;
+                bool got = mbar_wait(bar_tfull + 8 * b, tph, ERR_TIMEOUT_CONSUMER, &s_abort);
+                got = got && mbar_wait(bar_sbfull + 8 * s, (c / SB_STAGES) & 1, ERR_TIMEOUT_CONSUMER, &s_abort);
+                if (!__all_sync(0xFFFFFFFFu, got))
+                    return false;
+                tc_fence_after();
+                if (!dbg_ok(b * BN + col0 + 128 <= L::TMEM_COLS, DBG_GEMM_TMEM))
+                    return false;
+                const uint32_t tb = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * BN + col0;
+                const float *sbr = sbrow_smem + s * BN + col0 + p2;
+                uint64_t sa2[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    asm("mov.b64 %0, {%1, %1};" : "=l"(sa2[i]) : "f"(sa[i]));
+                uint32_t ra[16], rb[16];
+                tmem_ld16x4(tb, ra);                 // rows +0, +8;   columns 0..31
+                tmem_ld16x4(tb + (16u << 16), rb);   // rows +16, +24; columns 0..31
+                tmem_ld_wait_regs16x2(ra, rb);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float2 sbp[4];
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        sbp[jj] = *reinterpret_cast<const float2 *>(sbr + 32 * q + 8 * jj);
+                    fold4(0, q, ra, sbp, sa2);
+                    if (q < 3)
+                        tmem_ld16x4(tb + 32 * (q + 1), ra);
+                    fold4(1, q, rb, sbp, sa2);
+                    if (q < 3) {
+                        tmem_ld16x4(tb + (16u << 16) + 32 * (q + 1), rb);
+                        tmem_ld_wait_regs16x2(ra, rb);
+                    }
+                }
+                // freed after the last fold (see the race noted above)
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar_tempty + 8 * b);
+                    mbar_arrive(bar_sbempty + 8 * s);
+                }
+                ++c;
+            }
+            // epilogue: two columns per store, straight from the registers
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int m = rbase + 8 * i;
+                if (m >= tl.m_end)
+                    continue;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int n = tl.n0 + col0 + 8 * k + p2;
+                    if (n < p.N && dbg_ok(m < p.M && n + 2 <= p.N && p.N <= p.ldc, DBG_GEMM_STORE)) {
+                        const int64_t off = static_cast<int64_t>(m) * p.ldc + n;
+                        if constexpr (OUT_F32)
+                            *reinterpret_cast<float2 *>(reinterpret_cast<float *>(p.C) + off) =
+                                make_float2(acc[32 * i + 2 * k], acc[32 * i + 2 * k + 1]);
+                        else
+                            *reinterpret_cast<uint32_t *>(reinterpret_cast<uint16_t *>(p.C) + off) =
+                                pack_bf16x2(acc[32 * i + 2 * k], acc[32 * i + 2 * k + 1]);
+                    }
+                }
+            }
+            if constexpr (SPLIT_OK) {
+                if (it.mode == ITEM_HEAD)
+                    split_head_publish();
+            }
+            return true;
+        };
+        (void)item_rs16;
+
         Item it;
         for (int j = 0; ok && item_of<SPLIT_OK>(j, blockIdx.x, gridDim.x, total_tiles, num_kb, run, it); ++j) {
             const Tile tl = tile_of<BN, GROUPED>(it.t, p, tile_start);
+            if constexpr (RS16) {
+                if (!item_rs16(tl, it))
+                    ok = false;
+                continue;
+            }
             const int m_row = min(tl.m0 + row, p.M - 1);
             const float *sa_ptr = p.sa + m_row;
             // CPW columns starting at a multiple of CPW never straddle a
@@ -616,15 +811,8 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
             if constexpr (SPLIT_OK) {
                 if (it.mode == ITEM_TAIL) {
                     // continue from the accumulators CTA b+1 stored for this
-                    // tile's first chunks (one thread waits for its flag)
-                    bool got = true;
-                    if (threadIdx.x == kFirstPromoWarp * 32) {
-                        got = flag_wait(p.sk_flags + blockIdx.x, p.sk_epoch, ERR_TIMEOUT_SPLIT, &s_abort);
-                        if (got)
-                            mbar_arrive(bar_sktail);
-                    }
-                    got = mbar_wait(bar_sktail, 0, ERR_TIMEOUT_SPLIT, &s_abort);
-                    if (!__all_sync(0xFFFFFFFFu, got)) {
+                    // tile's first chunks
+                    if (!split_tail_wait()) {
                         ok = false;
                         break;
                     }
@@ -721,28 +909,8 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                     release();
                     fold(0, ra);
                     fold(1, rb);
-                } else if constexpr (BMODE == 1) {
-                    // Row-scale folds are twice the work: fold the first two
-                    // pieces between the loads.  The buffer is freed only after
-                    // the last fold.  Freeing it as soon as the last loads had
-                    // been waited for (before the last two folds) let the next
-                    // chunk's MMAs corrupt this chunk's values in the first 8
-                    // lanes of the last columns, in about one launch in 20 of
-                    // the Wgrad workload (found by repeating it and comparing
-                    // outputs bit for bit); freeing it after the folds never
-                    // did in 2000 launches.
-                    tmem_ld32(tbase + pcol(0), ra);
-                    tmem_ld32(tbase + pcol(1), rb);
-                    tmem_ld_wait_regs2(ra, rb);
-                    fold(0, ra);
-                    tmem_ld32(tbase + pcol(2), ra);
-                    fold(1, rb);
-                    tmem_ld32(tbase + pcol(3), rb);
-                    tmem_ld_wait_regs2(ra, rb);
-                    fold(2, ra);
-                    fold(3, rb);
-                    release();
                 } else {
+                    // (per-row scales at 256 columns take the 16x256b path above)
                     // four loads, each overlapped with the fold of the previous one
                     tmem_ld32(tbase + pcol(0), ra);
                     tmem_ld_wait_regs(ra);
@@ -914,19 +1082,8 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                     __syncwarp();
                 }
                 if constexpr (SPLIT_OK) {
-                    if (it.mode == ITEM_HEAD) {
-                        // the partial is in C: publish it to CTA b-1 once every
-                        // promotion warp's stores are visible at GPU scope
-                        __threadfence();
-                        __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive(bar_skhead);
-                        if (threadIdx.x == kFirstPromoWarp * 32) {
-                            if (mbar_wait(bar_skhead, 0, ERR_TIMEOUT_SPLIT, &s_abort) &&
-                                dbg_ok(blockIdx.x >= 1, DBG_GEMM_SPLIT))
-                                flag_release(p.sk_flags + blockIdx.x - 1, p.sk_epoch);
-                        }
-                    }
+                    if (it.mode == ITEM_HEAD)  // the partial is in C
+                        split_head_publish();
                 }
             }
         }
