@@ -207,11 +207,9 @@ int launch_gemm_bn(int bn, int out_dtype, DeviceInfo *d, const CUtensorMap &tA, 
     if (bn == 256)
         return out_dtype == 0 ? launch_gemm<256, BMODE, false, GROUPED>(d, tA, tB, tSB, p, grid, st)
                               : launch_gemm<256, BMODE, true, GROUPED>(d, tA, tB, tSB, p, grid, st);
-    if constexpr (BMODE == 0) {
-        if (bn == 192)
-            return out_dtype == 0 ? launch_gemm<192, BMODE, false, GROUPED>(d, tA, tB, tSB, p, grid, st)
-                                  : launch_gemm<192, BMODE, true, GROUPED>(d, tA, tB, tSB, p, grid, st);
-    }
+    if (bn == 192)
+        return out_dtype == 0 ? launch_gemm<192, BMODE, false, GROUPED>(d, tA, tB, tSB, p, grid, st)
+                              : launch_gemm<192, BMODE, true, GROUPED>(d, tA, tB, tSB, p, grid, st);
     return out_dtype == 0 ? launch_gemm<128, BMODE, false, GROUPED>(d, tA, tB, tSB, p, grid, st)
                           : launch_gemm<128, BMODE, true, GROUPED>(d, tA, tB, tSB, p, grid, st);
 }
@@ -270,8 +268,7 @@ int pick_bn(int64_t M, int64_t N, int b_scale_mode, int num_sms)
     (void)num_sms;
     const int forced = g_tile_n.load(std::memory_order_relaxed);
     if (b_scale_mode != 0) {
-        // Per-row B scales are built for the 128 and 256 widths only.
-        if (forced == 128 || forced == 256)
+        if (forced)
             return forced;
         return N > 128 ? 256 : 128;
     }

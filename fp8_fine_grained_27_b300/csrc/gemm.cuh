@@ -651,13 +651,16 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
         // let the next chunk's MMAs corrupt this chunk's values (in about one
         // launch in 20 of the Wgrad workload, found by repeating it and
         // comparing outputs bit for bit; never after the last fold).
-        constexpr bool RS16 = (BMODE == 1 && BN == 256);
+        constexpr bool RS16 = (BMODE == 1 && BN >= 192);
+        constexpr int KP = L::CPW / 8;   // column pairs per row of a thread
+        constexpr int AR = 2 * KP;       // accumulators per row of a thread
+        constexpr int NQ = L::CPW / 32;  // 32-column quarters of a warpgroup's columns
         auto item_rs16 = [&](const Tile &tl, const Item &it) -> bool {
             const int t4 = lane >> 2, p2 = (lane & 3) * 2;
             const int rbase = tl.m0 + quarter * 32 + t4;  // rows rbase + 8i
-            float acc[128];
+            float acc[4 * AR];
 #pragma unroll
-            for (int j = 0; j < 128; ++j)
+            for (int j = 0; j < 4 * AR; ++j)
                 acc[j] = 0.0f;
             if constexpr (SPLIT_OK) {
                 if (it.mode == ITEM_TAIL) {
@@ -670,12 +673,12 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                             continue;
                         const float *crow = reinterpret_cast<const float *>(p.C) + static_cast<int64_t>(m) * p.ldc;
 #pragma unroll
-                        for (int k = 0; k < 16; ++k) {
+                        for (int k = 0; k < KP; ++k) {
                             const int n = tl.n0 + col0 + 8 * k + p2;
                             if (n < p.N && dbg_ok(m < p.M && n + 2 <= p.N && p.N <= p.ldc, DBG_GEMM_SPLIT)) {
                                 const float2 v = __ldcg(reinterpret_cast<const float2 *>(crow + n));
-                                acc[32 * i + 2 * k] = v.x;
-                                acc[32 * i + 2 * k + 1] = v.y;
+                                acc[AR * i + 2 * k] = v.x;
+                                acc[AR * i + 2 * k + 1] = v.y;
                             }
                         }
                     }
@@ -703,10 +706,10 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                         const int i = 2 * h + ri, k = 4 * q + jj;
                         uint64_t sc2, a2, p2v;
                         asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(sc2) : "l"(sa2[i]), "l"(sb2));
-                        asm("mov.b64 %0, {%1, %2};" : "=l"(a2) : "f"(acc[32 * i + 2 * k]), "f"(acc[32 * i + 2 * k + 1]));
+                        asm("mov.b64 %0, {%1, %2};" : "=l"(a2) : "f"(acc[AR * i + 2 * k]), "f"(acc[AR * i + 2 * k + 1]));
                         asm("mov.b64 %0, {%1, %2};" : "=l"(p2v) : "r"(r[4 * jj + 2 * ri]), "r"(r[4 * jj + 2 * ri + 1]));
                         asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a2) : "l"(sc2), "l"(p2v));
-                        asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[32 * i + 2 * k]), "=f"(acc[32 * i + 2 * k + 1]) : "l"(a2));
+                        asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[AR * i + 2 * k]), "=f"(acc[AR * i + 2 * k + 1]) : "l"(a2));
                     }
                 }
             };
@@ -721,7 +724,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                 if (!__all_sync(0xFFFFFFFFu, got))
                     return false;
                 tc_fence_after();
-                if (!dbg_ok(b * BN + col0 + 128 <= L::TMEM_COLS, DBG_GEMM_TMEM))
+                if (!dbg_ok(b * BN + col0 + L::CPW <= L::TMEM_COLS, DBG_GEMM_TMEM))
                     return false;
                 const uint32_t tb = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + b * BN + col0;
                 const float *sbr = sbrow_smem + s * BN + col0 + p2;
@@ -734,16 +737,16 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                 tmem_ld16x4(tb + (16u << 16), rb);   // rows +16, +24; columns 0..31
                 tmem_ld_wait_regs16x2(ra, rb);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < NQ; ++q) {
                     float2 sbp[4];
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj)
                         sbp[jj] = *reinterpret_cast<const float2 *>(sbr + 32 * q + 8 * jj);
                     fold4(0, q, ra, sbp, sa2);
-                    if (q < 3)
+                    if (q < NQ - 1)
                         tmem_ld16x4(tb + 32 * (q + 1), ra);
                     fold4(1, q, rb, sbp, sa2);
-                    if (q < 3) {
+                    if (q < NQ - 1) {
                         tmem_ld16x4(tb + (16u << 16) + 32 * (q + 1), rb);
                         tmem_ld_wait_regs16x2(ra, rb);
                     }
@@ -764,16 +767,16 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                 if (m >= tl.m_end)
                     continue;
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
+                for (int k = 0; k < KP; ++k) {
                     const int n = tl.n0 + col0 + 8 * k + p2;
                     if (n < p.N && dbg_ok(m < p.M && n + 2 <= p.N && p.N <= p.ldc, DBG_GEMM_STORE)) {
                         const int64_t off = static_cast<int64_t>(m) * p.ldc + n;
                         if constexpr (OUT_F32)
                             *reinterpret_cast<float2 *>(reinterpret_cast<float *>(p.C) + off) =
-                                make_float2(acc[32 * i + 2 * k], acc[32 * i + 2 * k + 1]);
+                                make_float2(acc[AR * i + 2 * k], acc[AR * i + 2 * k + 1]);
                         else
                             *reinterpret_cast<uint32_t *>(reinterpret_cast<uint16_t *>(p.C) + off) =
-                                pack_bf16x2(acc[32 * i + 2 * k], acc[32 * i + 2 * k + 1]);
+                                pack_bf16x2(acc[AR * i + 2 * k], acc[AR * i + 2 * k + 1]);
                     }
                 }
             }

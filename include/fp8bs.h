@@ -326,9 +326,7 @@ int fp8bs_selftest_division(unsigned long long *counts, void *stream);
  * entry points for block-scaled B: 128, 192 or 256, or 0 to let the library
  * choose from the problem shape (the default).  Process-wide; results do not
  * depend on it (every output element is computed the same way), only speed.
- * Per-row B scales (b_scale_mode 1) come in widths 128 and 256 only; a
- * forced 192 leaves them on the automatic choice.  fp8_gemm_ue8m0 uses 256
- * unless 192 is forced.
+ * fp8_gemm_ue8m0 uses 256 unless 192 is forced.
  */
 int fp8bs_set_gemm_tile_n(int bn);
 
