@@ -541,6 +541,10 @@ int fp8_gemm_blockscaled(const uint8_t *A, int64_t lda, const float *sa, int64_t
     const int BN = pick_bn(M, N, b_scale_mode, d->num_sms);
     p.tile_n = BN;
     p.b_rows = static_cast<int>(N);
+    // per-row scales at the wide tiles: the A row scales of a chunk are
+    // copied into shared memory with its B scale row when that is a legal
+    // bulk copy (16-byte aligned rows, a multiple of 16 bytes)
+    p.sa_smem = (b_scale_mode == 1 && BN >= 192 && aligned16(sa) && ldsa % 4 == 0 && M % 4 == 0) ? 1 : 0;
     CUtensorMap tA, tB, tSB;
     std::memset(&tSB, 0, sizeof tSB);
     if (make_map(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, lda, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||

@@ -106,7 +106,8 @@ struct Cfg {
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = BN * BK;
     static constexpr int SBROW_BYTES = (BMODE_ == 1) ? BN * 4 : 0;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SBROW_BYTES;
+    static constexpr int SAROW_BYTES = (BMODE_ == 1) ? BM * 4 : 0;  // the chunk's A row scales (Params::sa_smem)
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SBROW_BYTES + SAROW_BYTES;
     static constexpr int EPI_BYTES = NPW * 2048;
     static constexpr int TABLE_BYTES = GROUPED_ ? (kMaxGroups + 1) * 4 : 0;
     static constexpr int XCH_BYTES = 2048;  // SwiGLU row-amax exchange, two tiles deep
@@ -125,7 +126,8 @@ struct Cfg {
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SBROW = OFF_B + STAGES * B_BYTES;
-    static constexpr int OFF_EPI = OFF_SBROW + SB_STAGES * SBROW_BYTES;
+    static constexpr int OFF_SAROW = OFF_SBROW + SB_STAGES * SBROW_BYTES;
+    static constexpr int OFF_EPI = OFF_SAROW + SB_STAGES * SAROW_BYTES;
     static constexpr int OFF_XCH = OFF_EPI + EPI_BYTES;
     static constexpr int OFF_BAR = OFF_XCH + XCH_BYTES;
     static constexpr int NBAR = 2 * STAGES + 2 * SB_STAGES + 2 * NTMEM + 3;  // + SwiGLU exchange, two K-split
@@ -157,6 +159,12 @@ struct Params {
     int sk_first = 0x7FFFFFFF;  // first tile shared out by K chunks (dense FP32 output); none by default
     uint32_t *sk_flags = nullptr;  // flag of the tile split between CTA b and b+1: sk_flags[b]
     uint32_t sk_epoch = 0;         // this launch's flag value (never 0)
+    // BMODE 1 at BN >= 192: the producer copies each chunk's A row scales
+    // (sa[kb*ldsa + m0 ..], min(128, M - m0) floats) into the chunk's scale
+    // slot beside its B scale row; the host sets it when sa is 16-byte
+    // aligned and ldsa and M are multiples of 4, so that the copy is a
+    // legal bulk copy
+    int sa_smem = 0;
 };
 
 // One piece of work of a CTA: tile t, K chunks [kb0, kb1).
@@ -529,9 +537,17 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                             break;
                         }
                         sb_issued = c + 1;
-                        mbar_arrive_expect_tx(bar_sbfull + 8 * q, L::SBROW_BYTES);
+                        // the A row scales ride on the same barrier (rows past M are not copied)
+                        uint32_t sab = p.sa_smem ? static_cast<uint32_t>(min(BM, p.M - tl.m0)) * 4u : 0u;
+                        if (sab != 0 &&
+                            !dbg_ok(sab % 16 == 0 && tl.m0 + sab / 4 <= p.ldsa && kb < p.K / BK, DBG_GEMM_SCALE_A))
+                            sab = 0;
+                        mbar_arrive_expect_tx(bar_sbfull + 8 * q, L::SBROW_BYTES + sab);
                         tma_load_2d(sbase + L::OFF_SBROW + q * L::SBROW_BYTES, &tmSB, tl.n0, kb,
                                     bar_sbfull + 8 * q);
+                        if (sab != 0)
+                            bulk_load(sbase + L::OFF_SAROW + q * L::SAROW_BYTES,
+                                      p.sa + static_cast<int64_t>(kb) * p.ldsa + tl.m0, sab, bar_sbfull + 8 * q);
                     }
                 }
             }
@@ -713,9 +729,16 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                     }
                 }
             };
+            const float *sarow_smem = reinterpret_cast<const float *>(smem + L::OFF_SAROW) + quarter * 32 + t4;
             for (int kb = it.kb0; kb < it.kb1; ++kb) {
+                // the row scales come with the chunk's scale slot (a bulk copy
+                // by the producer, issued chunks ahead) or, where that copy is
+                // not allowed, straight from global memory; the global loads
+                // stood on the loop's critical path (knocked out in a probe
+                // copy, the Wgrad GEMM ran 12% faster)
                 float sa[4];
-                ld_sa4(kb, sa);
+                if (!p.sa_smem)
+                    ld_sa4(kb, sa);
                 const int b = c % NTMEM;
                 const uint32_t tph = (c / NTMEM) & 1;
                 const int s = c % SB_STAGES;
@@ -723,6 +746,11 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                 got = got && mbar_wait(bar_sbfull + 8 * s, (c / SB_STAGES) & 1, ERR_TIMEOUT_CONSUMER, &s_abort);
                 if (!__all_sync(0xFFFFFFFFu, got))
                     return false;
+                if (p.sa_smem) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        sa[i] = sarow_smem[s * BM + 8 * i];
+                }
                 tc_fence_after();
                 if (!dbg_ok(b * BN + col0 + L::CPW <= L::TMEM_COLS, DBG_GEMM_TMEM))
                     return false;

@@ -172,7 +172,13 @@ int fp8_gemm_ue8m0(const uint8_t *A, int64_t lda, const float *sa, int64_t ldsa,
  *                   128x128 block of B (weights; Fprop and Dgrad).
  *                1: sb FP32 [K/128][ldsb], ldsb >= N, ldsb % 4 == 0: one scale
  *                   per row of B per 128 K (both operands tiled 1x128 along
- *                   K, as in the weight-gradient GEMM).
+ *                   K, as in the weight-gradient GEMM).  When sa is 16-byte
+ *                   aligned and ldsa and M are multiples of 4 (a dense
+ *                   [K/128][M] scale array from fp8_quant_1x128 along=1
+ *                   is, since that quantiser needs M % 8 == 0), the
+ *                   kernel stages each chunk's row scales in shared memory
+ *                   with a bulk copy; otherwise it reads them from global
+ *                   memory.  The result is the same either way.
  *   C   [M][ldc]; out_dtype 0: BF16 (round to nearest even), 1: FP32.
  *   Result: for each 128-wide K chunk kb the tensor cores form the FP32
  *   partial P_kb of the E4M3 products, and

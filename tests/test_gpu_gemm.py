@@ -165,11 +165,37 @@ def test_wgrad_small_full(fb, orc, tile_n):
     _wgrad(fb, orc, d["dY"], d["X"], what="wgrad small")
 
 
-@pytest.mark.parametrize("Cout,Cin,T", [(128, 8, 128), (384, 264, 384), (256, 136, 256)])
+@pytest.mark.parametrize("Cout,Cin,T", [(128, 8, 128), (384, 264, 384), (256, 136, 256), (200, 264, 256)])
 def test_wgrad_ragged(fb, orc, tile_n, Cout, Cin, T):
-    """Per-row B scales on output widths that end inside a tile."""
+    """Per-row B scales on output widths that end inside a tile (and, at Cout = 200, a last
+    row tile of 72 rows, whose row scales are bulk-copied short)."""
     d = synth.wgrad(T=T, Cout=Cout, Cin=Cin)
     _wgrad(fb, orc, d["dY"], d["X"], what=f"wgrad {Cout}x{Cin}x{T}")
+
+
+@pytest.mark.parametrize("layout", ["odd_ld", "offset"])
+def test_wgrad_row_scales_global_path(fb, tile_n, layout):
+    """A row-scale layout that cannot be bulk-copied into shared memory (a row pitch that is
+    not a multiple of 4 floats, or a base 4 bytes off a 16-byte boundary) takes the
+    global-load path; the result must be bit-identical to the staged path's."""
+    d = synth.wgrad(T=1024, Cout=256, Cin=392)
+    qdy, sdy = fb.quant_1x128(dev(d["dY"]), along=1)
+    qx, sx = fb.quant_1x128(dev(d["X"]), along=1)
+    C0 = torch.empty((256, 392), dtype=torch.float32, device="cuda")
+    fb.gemm_blockscaled(qdy, sdy, qx, sx, 1, C=C0)
+    nkb, M = sdy.shape
+    if layout == "odd_ld":
+        buf = torch.full((nkb, M + 1), float("nan"), dtype=torch.float32, device="cuda")
+        s2 = buf[:, :M]
+    else:
+        buf = torch.full((nkb * (M + 4) + 1,), float("nan"), dtype=torch.float32, device="cuda")
+        s2 = buf[1:].view(nkb, M + 4)[:, :M]
+    s2.copy_(sdy)
+    C1 = torch.full_like(C0, float("nan"))
+    fb.gemm_blockscaled(qdy, s2, qx, sx, 1, C=C1)
+    torch.cuda.synchronize()
+    assert fb.get_device_error() == 0
+    assert torch.equal(C0.view(torch.int32), C1.view(torch.int32)), f"{layout}: staged and global row scales differ"
 
 
 def test_wgrad_full_size(fb, orc):
