@@ -159,7 +159,7 @@ struct Params {
     int sk_first = 0x7FFFFFFF;  // first tile shared out by K chunks (dense FP32 output); none by default
     uint32_t *sk_flags = nullptr;  // flag of the tile split between CTA b and b+1: sk_flags[b]
     uint32_t sk_epoch = 0;         // this launch's flag value (never 0)
-    // BMODE 1 at BN >= 192: the producer copies each chunk's A row scales
+    // BMODE 1: the producer copies each chunk's A row scales
     // (sa[kb*ldsa + m0 ..], min(128, M - m0) floats) into the chunk's scale
     // slot beside its B scale row; the host sets it when sa is 16-byte
     // aligned and ldsa and M are multiples of 4, so that the copy is a
@@ -652,12 +652,12 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
         (void)split_tail_wait;
         (void)split_head_publish;
 
-        // ---------------------------------- per-row scales at 256 columns
-        // The partial is read from TMEM in the 16x256b shape, eight pieces of
-        // 16 registers: a thread holds rows quarter*32 + 8i + lane/4 (i = 0..3)
-        // and the column pairs col0 + 8k + 2(lane%4) (k = 0..15) of its
-        // warpgroup's 128 columns, acc[32i + 2k + e].  It then needs 32 of the
-        // chunk's B scales instead of 128.  With one row and 128 columns per
+        // ---------------------------------- per-row scales (every tile width)
+        // The partial is read from TMEM in the 16x256b shape, pieces of 16
+        // registers: a thread holds rows quarter*32 + 8i + lane/4 (i = 0..3)
+        // and the column pairs col0 + 8k + 2(lane%4) (k < CPW/8) of its
+        // warpgroup's CPW columns, acc[AR*i + 2k + e].  At CPW = 128 it then
+        // needs 32 of the chunk's B scales instead of 128.  With one row and 128 columns per
         // thread every lane read all 128 as 16-byte shared-memory broadcasts,
         // about five wavefronts each, and those loads kept the shared-memory
         // data pipe 59% busy (ncu, Wgrad GEMM) beside the MMAs' operand reads.
@@ -667,7 +667,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
         // let the next chunk's MMAs corrupt this chunk's values (in about one
         // launch in 20 of the Wgrad workload, found by repeating it and
         // comparing outputs bit for bit; never after the last fold).
-        constexpr bool RS16 = (BMODE == 1 && BN >= 192);
+        constexpr bool RS16 = (BMODE == 1);
         constexpr int KP = L::CPW / 8;   // column pairs per row of a thread
         constexpr int AR = 2 * KP;       // accumulators per row of a thread
         constexpr int NQ = L::CPW / 32;  // 32-column quarters of a warpgroup's columns
@@ -941,7 +941,7 @@ __global__ void __launch_bounds__(Cfg<BN, BMODE, GROUPED>::THREADS, 1)
                     fold(0, ra);
                     fold(1, rb);
                 } else {
-                    // (per-row scales at 256 columns take the 16x256b path above)
+                    // (per-row scales take the 16x256b path above)
                     // four loads, each overlapped with the fold of the previous one
                     tmem_ld32(tbase + pcol(0), ra);
                     tmem_ld_wait_regs(ra);

@@ -110,9 +110,30 @@ __device__ __forceinline__ bool dbg_ok(bool in_bounds, int site)
 // error that an earlier launch left in the device error word does not make
 // later launches give up.  A null `abort` (a drain that must run to its own
 // limit) never gives up early and raises nothing.
+// Non-blocking test of a phase (no suspension).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// The phase is tested once without suspending before the (suspending)
+// try_wait loop: a try_wait on a phase that has already completed measured
+// about 200 cycles, and the GEMM loops wait on many such phases (operands
+// loaded chunks ahead, scale slots).  Wgrad GEMM 0.3686 -> 0.3400 ms, FFN
+// GEMM +1% at equal clock, bit-identical.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int code, volatile int *abort,
                                           uint64_t limit_ns = 2000000000ull)
 {
+    if (mbar_test_wait(bar, parity))
+        return true;
 #pragma unroll 1
     for (int i = 0; i < 256; ++i)
         if (mbar_try_wait(bar, parity))

@@ -330,8 +330,10 @@ int fp8bs_selftest_division(unsigned long long *counts, void *stream);
 /*
  * fp8bs_set_gemm_tile_n -- output tile width (N per CTA tile) of the GEMM
  * entry points for block-scaled B: 128, 192 or 256, or 0 to let the library
- * choose from the problem shape (the default).  Process-wide; results do not
- * depend on it (every output element is computed the same way), only speed.
+ * choose from the problem shape (the default: 128 when N <= 128, else 256
+ * with b_scale_mode 0 and 192 with b_scale_mode 1).  Process-wide; results
+ * do not depend on it (every output element is computed the same way), only
+ * speed.
  * fp8_gemm_ue8m0 uses 256 unless 192 is forced.
  */
 int fp8bs_set_gemm_tile_n(int bn);

@@ -71,11 +71,11 @@ def main():
     _, _, qwt, swt = fb.quant_128x128_t(dev(d["W"]))
     fb.gemm_blockscaled(qdy, sdy, qwt, swt, 0)
     clear("dgrad 129x128x256")
-    for Cout, Cin, T in [(128, 8, 128), (384, 264, 384)]:
+    for Cout, Cin, T in [(128, 8, 128), (384, 264, 384), (200, 264, 256)]:  # 200: a short last row tile
         w = synth.wgrad(T=T, Cout=Cout, Cin=Cin)
         qd, sd = fb.quant_1x128(dev(w["dY"]), along=1)
         qx, sx = fb.quant_1x128(dev(w["X"]), along=1)
-        for tn in (0, 128, 256):
+        for tn in (0, 128, 192, 256):
             fb.set_gemm_tile_n(tn)
             dW = fb.gemm_blockscaled(qd, sd, qx, sx, 1, out_dtype=torch.float32)
             torch.cuda.synchronize()

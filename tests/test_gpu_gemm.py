@@ -224,11 +224,11 @@ def _split_vs_whole(fb, run, M, N, what):
     return outs[0]
 
 
-@pytest.mark.parametrize("bn", [0, 128])
+@pytest.mark.parametrize("bn", [0, 128, 256])
 def test_split_last_round_wgrad_full(fb, bn):
-    """Workload 4 has 448 tiles of 128x256 (896 of 128x128) on 148 CTAs: its
-    last round is shared out by K chunks, and the result must equal the
-    whole-tile result bit for bit."""
+    """Workload 4 has 608 tiles of 128x192 (896 of 128x128, 448 of 128x256) on
+    148 CTAs: its last round is shared out by K chunks, and the result must
+    equal the whole-tile result bit for bit."""
     d = synth.wgrad()
     qdy, sdy = fb.quant_1x128(dev(d["dY"]), along=1)
     qx, sx = fb.quant_1x128(dev(d["X"]), along=1)
@@ -239,7 +239,7 @@ def test_split_last_round_wgrad_full(fb, bn):
         fb.set_gemm_tile_n(0)
 
 
-@pytest.mark.parametrize("bn", [0, 128])
+@pytest.mark.parametrize("bn", [0, 128, 256])
 @pytest.mark.parametrize("mode", ["row_scales", "block_scales"])
 def test_split_last_round_small(fb, orc, bn, mode):
     """160 (or 320) tiles and 3 K chunks: every CTA's run crosses tiles, so
@@ -270,8 +270,9 @@ def test_split_last_round_small(fb, orc, bn, mode):
     assert_gemm_close(host_bits(got), ref, f"split {mode} bn={bn}")
 
 
-@pytest.mark.parametrize("workload,launches", [("wgrad", 300), ("mla", 300), ("ffn", 40)])
-def test_repeated_launches_are_bit_identical(fb, workload, launches):
+@pytest.mark.parametrize("workload,launches,bn", [("wgrad", 300, 0), ("wgrad", 200, 128), ("wgrad", 200, 256),
+                                                  ("mla", 300, 0), ("ffn", 40, 0)])
+def test_repeated_launches_are_bit_identical(fb, workload, launches, bn):
     """The same GEMM launched many times into a NaN-filled output gives the
     same bits every time.  A race between a partial buffer's release and its
     reads showed up only this way: a few 8x4 blocks of the Wgrad output were
@@ -290,15 +291,19 @@ def test_repeated_launches_are_bit_identical(fb, workload, launches):
     C = torch.empty((qa.shape[0], qb.shape[0]), dtype=dtype, device="cuda")
     bits = torch.int32 if dtype == torch.float32 else torch.int16
     first, differ = None, 0
-    for _ in range(launches):
-        C.fill_(float("nan"))
-        fb.gemm_blockscaled(qa, sa, qb, sb, bmode, C=C)
-        if first is None:
-            first = C.view(bits).clone()
-        elif not torch.equal(C.view(bits), first):
-            differ += 1
+    fb.set_gemm_tile_n(bn)
+    try:
+        for _ in range(launches):
+            C.fill_(float("nan"))
+            fb.gemm_blockscaled(qa, sa, qb, sb, bmode, C=C)
+            if first is None:
+                first = C.view(bits).clone()
+            elif not torch.equal(C.view(bits), first):
+                differ += 1
+    finally:
+        fb.set_gemm_tile_n(0)
     assert fb.get_device_error() == 0
-    assert differ == 0, f"{workload}: {differ} of {launches - 1} launches differ from the first"
+    assert differ == 0, f"{workload} bn={bn}: {differ} of {launches - 1} launches differ from the first"
 
 
 @pytest.mark.parametrize("kind", ["grouped", "grouped_swiglu", "ue8m0_bf16", "ue8m0_fp32"])
