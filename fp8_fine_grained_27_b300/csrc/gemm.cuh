@@ -27,8 +27,10 @@
 //             (four 32-column TMEM loads per chunk, software-pipelined);
 //   BN = 192: 3 promotion warpgroups x 64 columns, 2 TMEM partials;
 //   BN = 128: 2 promotion warpgroups x 64 columns, 4 TMEM partials.
-//   With 64 columns per thread both 32-column loads of a chunk are issued
-//   before a single wait.
+//   With block scales and 64 columns per thread both 32-column loads of a
+//   chunk are issued before a single wait.  Per-row scales (BMODE 1) read the
+//   partial in the 16x256b shape at every width (see the promotion below);
+//   the library picks 256 for block scales and 192 for per-row scales.
 //
 // Synchronisation (all mbarriers, all waits bounded):
 //   full[s]   TMA bytes of stage s landed          (producer -> MMA)
@@ -39,8 +41,8 @@
 //             the promotion when it has folded the chunk
 //
 // The last round of tiles (FP32 output).  When the tiles do not fill the
-// last round of the persistent grid (Wgrad: 448 tiles on 148 CTAs is three
-// rounds and four tiles), the tiles from the second-to-last round on are
+// last round of the persistent grid (Wgrad: 608 tiles of 128 x 192 on 148
+// CTAs is four rounds and 16 tiles), the tiles from the second-to-last round on are
 // shared out by K chunks instead: CTA b takes the b-th of G equal runs of
 // their chunks, in tile order, so every CTA does the same number of chunks.
 // A tile then falls to at most two CTAs (every run is longer than a tile).
