@@ -104,10 +104,15 @@ int current_device(DeviceInfo **out)
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.quant_pair_ctas, quant::quant_pair_kernel<false>,
                                                               quant::kThreads, 0) != cudaSuccess)
                 return FP8BS_ECUDA;
+            if (cudaFuncSetAttribute(quant::quant_t_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     quant::kQtDynSmem) != cudaSuccess ||
+                cudaFuncSetAttribute(quant::quant_t_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     quant::kQtDynSmem) != cudaSuccess)
+                return FP8BS_ECUDA;
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.quant_cols_ctas, quant::quant_t_kernel<false>,
-                                                              quant::kThreads, 0) != cudaSuccess ||
+                                                              quant::kThreads, quant::kQtDynSmem) != cudaSuccess ||
                 cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d.quant_blockt_ctas, quant::quant_t_kernel<true>,
-                                                              quant::kThreads, 0) != cudaSuccess)
+                                                              quant::kThreads, quant::kQtDynSmem) != cudaSuccess)
                 return FP8BS_ECUDA;
             if (!g_encode) {
                 void *fn = nullptr;
@@ -329,8 +334,11 @@ int fp8_quant_1x128(const void *x, int64_t M, int64_t K, int64_t ldx, int along,
             return FP8BS_EINVAL;
         const int64_t tiles = (M / 128) * ((K + 127) / 128);
         const int64_t grid = std::min<int64_t>(tiles, int64_t(d->num_sms) * d->quant_cols_ctas);
-        quant::quant_t_kernel<false><<<static_cast<int>(grid), quant::kThreads, 0, st>>>(
-            static_cast<const uint16_t *>(x), M, K, ldx, nullptr, 0, q, ldq, s, lds, nullptr, 0);
+        CUtensorMap tmX;
+        if (make_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, ldx * 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return FP8BS_EINVAL;
+        quant::quant_t_kernel<false><<<static_cast<int>(grid), quant::kThreads, quant::kQtDynSmem, st>>>(
+            tmX, static_cast<const uint16_t *>(x), M, K, ldx, nullptr, 0, q, ldq, s, lds, nullptr, 0);
     }
     return launch_status();
 }
@@ -466,8 +474,12 @@ int fp8_quant_128x128_t(const void *w, int64_t N, int64_t K, int64_t ldw, uint8_
         return rc;
     const int64_t tiles = ((N + 127) / 128) * (K / 128);
     const int64_t grid = std::min<int64_t>(tiles, int64_t(d->num_sms) * d->quant_blockt_ctas);
-    quant::quant_t_kernel<true><<<static_cast<int>(grid), quant::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t *>(w), N, K, ldw, q, ldq, qt, ldqt, s, lds, st, ldst);
+    CUtensorMap tmW;
+    if (make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w, K, N, ldw * 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return FP8BS_EINVAL;
+    quant::quant_t_kernel<true><<<static_cast<int>(grid), quant::kThreads, quant::kQtDynSmem,
+                                  static_cast<cudaStream_t>(stream)>>>(
+        tmW, static_cast<const uint16_t *>(w), N, K, ldw, q, ldq, qt, ldqt, s, lds, st, ldst);
     return launch_status();
 }
 
